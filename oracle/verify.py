@@ -115,15 +115,19 @@ def block_tau(eta, h):
 
 
 def inverse_cdf(weights, u):
-    """(Y, margin): Y = smallest v with C(v) >= u * R; margin = distance of u*R to the
-    nearest of C(Y) and C(Y-1), relative to R (small margin = near tie)."""
+    """(Y, margin): Y = smallest v with C(v) >= u * R; margin = relative distance of u*R to
+    the two thresholds that decide Y, C(Y) and C(Y-1), each relative to the threshold itself
+    (a small margin is a near tie)."""
     c = np.cumsum(np.asarray(weights, np.float64))
     total = float(c[-1])
     t = u * total
     y = int(np.searchsorted(c, t, side="left"))
     y = min(y, len(c) - 1)
-    lo = float(c[y - 1]) if y > 0 else 0.0
-    margin = min(abs(t - float(c[y])), abs(t - lo)) / total
+    hi = float(c[y])
+    margin = abs(t - hi) / hi
+    if y > 0 and float(c[y - 1]) > 0.0:
+        lo = float(c[y - 1])
+        margin = min(margin, abs(t - lo) / lo)
     return y, margin
 
 
