@@ -1,0 +1,210 @@
+/*
+ * specverify.h - C ABI of the GB300 (sm_103a) speculative-decoding verify sampler.
+ *
+ * Four calls make up the hot path of one DSpark verify step:
+ *   dspark_markov_bias     - the Markov head's low-rank previous-token logit bias
+ *   spec_verify_tokenwise  - token-by-token speculative sampling
+ *   spec_verify_block      - block verification
+ *   adaptive_pick_k        - confidence head + the controller that picks how many drafts to verify
+ * Sources (web pages, cited by title and section):
+ *   [P1] "MTP, DSpark and Block Verification, Explained: Six Tokens per Step" (al-engr.com)
+ *   [P2] "MTP Heads and Confidence Heads: Linking Three Self-Drafting Routes into One Chain"
+ *        (naphjohn.github.io)
+ *   [P3] "Teaching the Speculator What a Draft Costs" (al-engr.com)
+ *
+ * Conventions shared by every call
+ *   - Every tensor argument is a DEVICE pointer to caller-owned memory, row-major and dense.
+ *     The library never allocates, never frees and never keeps a pointer after the call
+ *     returns.  It keeps no state between calls.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and never synchronises the host.  Outputs are valid once the stream reaches
+ *     the end of the call's work.  Calls on the same stream are ordered.
+ *   - Logit and weight dtypes are SPEC_DTYPE_F32 (float) or SPEC_DTYPE_BF16 (bfloat16).
+ *     Arithmetic is float32 per element with float64 per-stream scalars.
+ *   - Return value: SPEC_OK, or a negative SPEC_ERR_* for an error the host can see from the
+ *     arguments alone (nothing is launched then), or SPEC_ERR_CUDA when a launch failed.
+ *     spec_last_error() gives a one-line description of the last error in this host thread.
+ *   - Errors that depend on device data never trap the GPU: the verify calls write a
+ *     per-stream status code (SPEC_ST_*) and that stream emits nothing.
+ *   - Greedy rows: a stream whose temperature is exactly 0 takes the greedy branch in both
+ *     verify calls ([P1] §4 "Greedy is a different code path").
+ *   - Random numbers: Philox4x32-10 (Salmon et al., SC'11), key = (seed lo, seed hi),
+ *     counter = (slot, stream, step lo, step hi).  Output word 0 is the acceptance uniform
+ *     of draft slot `slot` (u_slot for the token-wise rule, eta_{slot+1} for block
+ *     verification); word 1 is the sampling uniform used when the step ends at `slot`.
+ *     U(x) = ((x >> 8) + 0.5) * 2^-24.  Same (seed, step) => bit-identical outputs.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPECVERIFY_VERSION 1
+
+/* dtypes */
+#define SPEC_DTYPE_F32 0
+#define SPEC_DTYPE_BF16 1
+
+/* host-visible return codes */
+#define SPEC_OK 0
+#define SPEC_ERR_ARG (-1)      /* NULL pointer or invalid enum value */
+#define SPEC_ERR_DTYPE (-2)    /* unsupported dtype combination */
+#define SPEC_ERR_SHAPE (-3)    /* size out of the supported range */
+#define SPEC_ERR_CUDA (-4)     /* a CUDA runtime call or launch failed */
+#define SPEC_ERR_DEVICE (-5)   /* the current device cannot run these kernels */
+
+/* per-stream status codes written by the verify calls (device data errors) */
+#define SPEC_ST_OK 0
+#define SPEC_ST_BAD_TEMPERATURE 1 /* T is NaN, infinite, negative, or positive but below FLT_MIN */
+#define SPEC_ST_BAD_TOKEN 2       /* a draft token of the stream lies outside [0, V) */
+#define SPEC_ST_BAD_ROW 3         /* a read logit row holds NaN or +inf, or has no finite entry */
+#define SPEC_ST_ZERO_DRAFT_PROB 4 /* T > 0 and q_i(x_i) = 0 (the draft logit at x_i is -inf) */
+#define SPEC_ST_BAD_OFFSETS 5     /* cu_drafts[b+1] - cu_drafts[b] is negative or above kmax */
+#define SPEC_ST_TIMEOUT 6         /* reserved: a bounded device wait gave up */
+#define SPEC_ST_NUMERIC 7         /* the distribution to draw from has zero or non-finite mass */
+
+/* limits */
+#define SPEC_MAX_KMAX 32          /* drafts per stream */
+#define SPEC_MAX_V 16777216       /* vocabulary size */
+
+/* columns of the optional diag output (one row per target row) */
+#define SPEC_DIAG_COLS 8
+#define SPEC_DIAG_PX 0     /* p_i(x_i) */
+#define SPEC_DIAG_QX 1     /* q_i(x_i) */
+#define SPEC_DIAG_W 2      /* block: clipped running product w_i (w_0 = 1) */
+#define SPEC_DIAG_H 3      /* block: threshold h_i, where it was evaluated */
+#define SPEC_DIAG_R 4      /* residual mass r_i, where it was computed */
+#define SPEC_DIAG_LOGZP 5  /* natural log of sum_v exp(l^p_i[v] / T) */
+#define SPEC_DIAG_LOGZQ 6  /* natural log of sum_v exp(l^q_i[v] / T) */
+#define SPEC_DIAG_RHO 7    /* rho_i = p_i(x_i) / q_i(x_i) */
+
+/*
+ * dspark_markov_bias - the Markov head's previous-token logit bias.
+ * [P2] §6 "Why the Markov Head Helps": B = W1 @ W2 (default rank 256), added to the current
+ * draft logits from the previous token; [P1] §3 "The Markov fix-up" and Figure 2: each
+ * slot's logits are biased by the token sampled one slot earlier (slot 0: the anchor).
+ *
+ *   out[r, v] = draft[r, v] + sum_{j < rank} W1[prev[r], j] * W2[j, v]     (float32)
+ *
+ * draft_logits [rows, V] (draft_dtype), prev_tokens [rows] int32, W1 [V, rank] and
+ * W2 [rank, V] (w_dtype), out_logits [rows, V] float32.  out may alias draft_logits only
+ * when draft_dtype is F32 (in place).  A row whose prev token lies outside [0, V) is written
+ * as all NaN (a later verify call reports it as SPEC_ST_BAD_ROW).
+ * Errors: SPEC_ERR_ARG (NULL pointer), SPEC_ERR_DTYPE, SPEC_ERR_SHAPE (rows < 0, V < 1,
+ * V > SPEC_MAX_V, rank < 1 or rank > 1024, or an alias with a bf16 input).
+ * rows == 0 launches nothing.
+ */
+int dspark_markov_bias(const void* draft_logits, int32_t draft_dtype, int32_t rows, int32_t V,
+                       const int32_t* prev_tokens, const void* W1, const void* W2,
+                       int32_t w_dtype, int32_t rank, float* out_logits, void* stream);
+
+/*
+ * Arguments shared by both verify calls.  B streams; stream b has
+ * N_b = cu_drafts[b+1] - cu_drafts[b] drafts (0 <= N_b <= kmax).
+ *   draft row of (b, i)  = cu_drafts[b] + i          (i < N_b)
+ *   target row of (b, i) = cu_drafts[b] + b + i      (i <= N_b; i = N_b is the bonus slot)
+ * Inputs (device): cu_drafts [B+1] int32; draft_logits [cu[B], V]; target_logits
+ * [cu[B] + B, V]; draft_tokens [cu[B]] int32; temperature [B] float (0 = greedy).
+ * Outputs (device, fully written for every stream): accepted_len [B] int32 (tau);
+ * out_tokens [B, kmax+1] int32 = x_0 .. x_{tau-1}, then the target's token, then -1;
+ * n_emitted [B] int32 = tau + 1 (0 when status != 0); status [B] int32 (SPEC_ST_*).
+ * diag is optional (NULL = not written): float [cu[B] + B, SPEC_DIAG_COLS], NaN where a
+ * value was not computed.
+ * Rows read: T > 0 reads all 2 N_b + 1 rows of the stream; T = 0 reads the N_b + 1 target
+ * rows only.  Status precedence: BAD_OFFSETS, BAD_TEMPERATURE, BAD_TOKEN, BAD_ROW,
+ * ZERO_DRAFT_PROB, NUMERIC.
+ * The caller must make the arrays at least as long as cu_drafts[B] implies; the kernels
+ * read cu_drafts on the device and cannot check buffer lengths.
+ */
+typedef struct {
+    int32_t B;
+    int32_t V;
+    int32_t kmax;
+    const int32_t* cu_drafts;
+    const void* draft_logits;
+    int32_t draft_dtype;
+    const void* target_logits;
+    int32_t target_dtype;
+    const int32_t* draft_tokens;
+    const float* temperature;
+    uint64_t seed;
+    uint64_t step;
+    int32_t* accepted_len;
+    int32_t* out_tokens;
+    int32_t* n_emitted;
+    int32_t* status;
+    float* diag;
+} spec_verify_args;
+
+/*
+ * spec_verify_tokenwise - token-by-token speculative sampling.
+ * [P1] §4 "Token by token" (Leviathan et al. 2023): walk the drafts in order and accept x_i
+ * while u_i <= min(1, p_i(x_i) / q_i(x_i)); at the first rejection j emit a token drawn
+ * from max(0, p_j - q_j) (normalised) and stop; if all N drafts pass emit the bonus drawn
+ * from p_N.  p_i = softmax(target_i / T), q_i = softmax(draft_i / T).  Draws are inverse
+ * CDF: the smallest v with C(v) >= U * R (ascending vocabulary order).
+ * Errors: SPEC_ERR_ARG, SPEC_ERR_DTYPE, SPEC_ERR_SHAPE (B < 0, V < 1, V > SPEC_MAX_V,
+ * kmax < 0 or kmax > SPEC_MAX_KMAX), SPEC_ERR_CUDA.  B == 0 launches nothing.
+ */
+int spec_verify_tokenwise(const spec_verify_args* args, void* stream);
+
+/*
+ * spec_verify_block - block verification.
+ * [P1] §4 "Block verification" (Sun et al. 2024) and Figure 3: with the clipped running
+ * product w_0 = 1, w_{i+1} = min(1, w_i p_i(x_i) / q_i(x_i)), the residual mass
+ * r_i = sum_v max(0, w_i p_i(v) - q_i(v)) and the threshold h_i = r_i / (r_i + 1 - w_i)
+ * (i < N; h_N = w_N; 0/0 reads as 1), the accepted length is tau = the last i >= 1 with
+ * eta_i <= h_i (0 if none); emit x_0 .. x_{tau-1} and a token drawn from
+ * max(0, w_tau p_tau - q_tau) (tau < N) or from p_N (tau = N).
+ * Errors: as spec_verify_tokenwise.
+ */
+int spec_verify_block(const spec_verify_args* args, void* stream);
+
+/*
+ * adaptive_pick_k - confidence head and adaptive verification.
+ * [P2] §7 "Only Then Comes the Confidence Head": c_k = sigmoid(h_k . w + bias);
+ * §9 "Why It Is Called Prefix Survival Probability": a_j = c_1 ... c_j;
+ * [P1] §6: a stream that verifies n drafts expects E_n = 1 + a_1 + ... + a_n tokens;
+ * [P3] "The controller, and the table it reads from": pick the count with the best
+ * expected tokens per millisecond, the cost read from verify_ms[num_tokens].
+ *   mode 0 (per stream): k_b = argmax_{n in 0..kmax} E_n / verify_ms[n + 1], ties -> smaller n.
+ *   mode 1 (batch, greedy in descending a - figure text after [P2] §9): order every (b, j)
+ *     by (a desc, b asc, j asc), m* = argmax_m (B + a-sum of the first m) / verify_ms[B + m]
+ *     (ties -> smaller m), k_b = the number of stream b's entries among the first m*.
+ * hidden [B, kmax, H] and w [H] in `dtype`; verify_ms [n_max + 1] float (index = tokens in
+ * the verify pass; index 0 unused).  Outputs: c_out [B, kmax] float, a_out [B, kmax] float,
+ * k_out [B] int32, cu_drafts_out [B + 1] int32 (exclusive prefix sum of k).
+ * Errors: SPEC_ERR_ARG (NULL pointer, mode not 0/1), SPEC_ERR_DTYPE, SPEC_ERR_SHAPE
+ * (B < 1, kmax < 1 or > SPEC_MAX_KMAX, H < 1, n_max < kmax + 1 in mode 0 or
+ * n_max < B * (kmax + 1) in mode 1, B * kmax > 4096 in mode 1), SPEC_ERR_CUDA.
+ */
+int adaptive_pick_k(const void* hidden, const void* w, int32_t dtype, float bias, int32_t B,
+                    int32_t kmax, int32_t H, const float* verify_ms, int32_t n_max,
+                    int32_t mode, float* c_out, float* a_out, int32_t* k_out,
+                    int32_t* cu_drafts_out, void* stream);
+
+/*
+ * spec_philox_uniforms - the verify calls' uniforms, exposed for checking.
+ * out [n_streams, n_slots, 2] double: (acceptance uniform, sampling uniform) of every
+ * (stream, slot) for the given seed and step, exactly as the verify kernels draw them.
+ * Errors: SPEC_ERR_ARG (NULL out), SPEC_ERR_SHAPE (a negative count), SPEC_ERR_CUDA.
+ */
+int spec_philox_uniforms(uint64_t seed, uint64_t step, int32_t n_streams, int32_t n_slots,
+                         double* out, void* stream);
+
+/* One-line description of the last error returned in the calling host thread ("" if none). */
+const char* spec_last_error(void);
+
+/* SPECVERIFY_VERSION of the loaded library. */
+int32_t spec_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,1 +1,250 @@
-"""GB300-native speculative-decoding verify sampler (placeholder; binding added with the library)."""
+"""GB300-native speculative-decoding verify sampler: Python binding of libspecverify.so.
+
+The binding only marshals arguments: it checks tensor devices, dtypes and shapes, passes raw
+device pointers and the current CUDA stream to the C ABI (``include/specverify.h``) and
+raises on a nonzero return code.  Every step of the method runs in the library's CUDA
+kernels; there is no fallback.  PyTorch supplies device memory and streams.
+
+Entry points (same names as the C ABI):
+
+* ``dspark_markov_bias``     - Markov head's low-rank previous-token logit bias
+* ``spec_verify_tokenwise``  - token-by-token speculative sampling
+* ``spec_verify_block``      - block verification
+* ``adaptive_pick_k``        - confidence head + pick how many drafts to verify
+* ``spec_philox_uniforms``   - the verify calls' uniforms (for checking)
+
+Build the library first: ``python -m speculative_decoding_block_verify_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+
+import ctypes
+import os
+
+__all__ = [
+    "dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block", "adaptive_pick_k",
+    "spec_philox_uniforms", "lib", "lib_path", "SpecError",
+    "DTYPE_F32", "DTYPE_BF16", "STATUS_NAMES", "DIAG_COLS",
+]
+
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+DIAG_COLS = 8
+STATUS_NAMES = {0: "OK", 1: "BAD_TEMPERATURE", 2: "BAD_TOKEN", 3: "BAD_ROW",
+                4: "ZERO_DRAFT_PROB", 5: "BAD_OFFSETS", 6: "TIMEOUT", 7: "NUMERIC"}
+EXPORTED = ["dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block",
+            "adaptive_pick_k", "spec_philox_uniforms", "spec_last_error", "spec_version"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+
+
+class SpecError(RuntimeError):
+    """A nonzero return code from the C ABI."""
+
+    def __init__(self, code, msg):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+class VerifyArgs(ctypes.Structure):
+    """Mirror of spec_verify_args."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("V", ctypes.c_int32), ("kmax", ctypes.c_int32),
+        ("cu_drafts", ctypes.c_void_p),
+        ("draft_logits", ctypes.c_void_p), ("draft_dtype", ctypes.c_int32),
+        ("target_logits", ctypes.c_void_p), ("target_dtype", ctypes.c_int32),
+        ("draft_tokens", ctypes.c_void_p), ("temperature", ctypes.c_void_p),
+        ("seed", ctypes.c_uint64), ("step", ctypes.c_uint64),
+        ("accepted_len", ctypes.c_void_p), ("out_tokens", ctypes.c_void_p),
+        ("n_emitted", ctypes.c_void_p), ("status", ctypes.c_void_p),
+        ("diag", ctypes.c_void_p),
+    ]
+
+
+def lib_path():
+    return os.path.join(_HERE, "_build", "libspecverify.so")
+
+
+def lib():
+    """Load libspecverify.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m speculative_decoding_block_verify_gb300.build`")
+    L = ctypes.CDLL(path)
+    vp, i32, u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64
+    L.dspark_markov_bias.argtypes = [vp, i32, i32, i32, vp, vp, vp, i32, i32, vp, vp]
+    L.spec_verify_tokenwise.argtypes = [ctypes.POINTER(VerifyArgs), vp]
+    L.spec_verify_block.argtypes = [ctypes.POINTER(VerifyArgs), vp]
+    L.adaptive_pick_k.argtypes = [vp, vp, i32, ctypes.c_float, i32, i32, i32, vp, i32, i32,
+                                  vp, vp, vp, vp, vp]
+    L.spec_philox_uniforms.argtypes = [u64, u64, i32, i32, vp, vp]
+    L.spec_last_error.restype = ctypes.c_char_p
+    L.spec_version.restype = ctypes.c_int32
+    for name in ("dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block",
+                 "adaptive_pick_k", "spec_philox_uniforms"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(rc):
+    if rc != 0:
+        raise SpecError(rc, lib().spec_last_error().decode())
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _dev(t, name, dtype=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else ctypes.c_void_p(0)
+
+
+def dspark_markov_bias(draft_logits, prev_tokens, W1, W2, out=None, stream=None):
+    """out[r, v] = draft[r, v] + sum_j W1[prev[r], j] W2[j, v] (float32 output).
+
+    draft_logits [rows, V] float32/bf16, prev_tokens [rows] int32, W1 [V, R], W2 [R, V]
+    (same dtype).  ``out`` may be ``draft_logits`` itself when that is float32.
+    """
+    torch = _torch()
+    _dev(draft_logits, "draft_logits")
+    _dev(prev_tokens, "prev_tokens", torch.int32)
+    _dev(W1, "W1")
+    _dev(W2, "W2")
+    rows, V = draft_logits.shape
+    R = W2.shape[0]
+    if W1.dtype != W2.dtype or tuple(W1.shape) != (V, R) or tuple(W2.shape) != (R, V):
+        raise ValueError("W1 must be [V, R] and W2 [R, V] with one dtype")
+    if prev_tokens.shape != (rows,):
+        raise ValueError("prev_tokens must be [rows]")
+    if out is None:
+        out = torch.empty((rows, V), dtype=torch.float32, device=draft_logits.device)
+    _dev(out, "out", torch.float32)
+    _check(lib().dspark_markov_bias(_ptr(draft_logits), _dtype_code(draft_logits), rows, V,
+                                    _ptr(prev_tokens), _ptr(W1), _ptr(W2), _dtype_code(W1), R,
+                                    _ptr(out), _stream(stream)))
+    return out
+
+
+def _verify(fn, cu_drafts, draft_logits, target_logits, draft_tokens, temperature, kmax, seed,
+            step, out=None, diag=False, stream=None):
+    torch = _torch()
+    _dev(cu_drafts, "cu_drafts", torch.int32)
+    _dev(target_logits, "target_logits")
+    _dev(draft_logits, "draft_logits")
+    _dev(draft_tokens, "draft_tokens", torch.int32)
+    _dev(temperature, "temperature", torch.float32)
+    B = cu_drafts.numel() - 1
+    V = target_logits.shape[1]
+    if draft_logits.dim() != 2 or (draft_logits.shape[0] > 0 and draft_logits.shape[1] != V):
+        raise ValueError("draft_logits must be [rows, V]")
+    if temperature.numel() != B:
+        raise ValueError("temperature must be [B]")
+    dev = target_logits.device
+    if out is None:
+        out = {
+            "accepted_len": torch.empty(B, dtype=torch.int32, device=dev),
+            "out_tokens": torch.empty((B, kmax + 1), dtype=torch.int32, device=dev),
+            "n_emitted": torch.empty(B, dtype=torch.int32, device=dev),
+            "status": torch.empty(B, dtype=torch.int32, device=dev),
+        }
+        if diag:
+            out["diag"] = torch.empty((target_logits.shape[0], DIAG_COLS), dtype=torch.float32,
+                                      device=dev)
+    a = VerifyArgs()
+    a.B, a.V, a.kmax = B, V, kmax
+    a.cu_drafts = cu_drafts.data_ptr()
+    a.draft_logits = draft_logits.data_ptr() if draft_logits.numel() else None
+    a.draft_dtype = _dtype_code(draft_logits)
+    a.target_logits = target_logits.data_ptr()
+    a.target_dtype = _dtype_code(target_logits)
+    a.draft_tokens = draft_tokens.data_ptr() if draft_tokens.numel() else None
+    a.temperature = temperature.data_ptr()
+    a.seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+    a.step = int(step) & 0xFFFFFFFFFFFFFFFF
+    a.accepted_len = out["accepted_len"].data_ptr()
+    a.out_tokens = out["out_tokens"].data_ptr()
+    a.n_emitted = out["n_emitted"].data_ptr()
+    a.status = out["status"].data_ptr()
+    a.diag = out["diag"].data_ptr() if out.get("diag") is not None else None
+    _check(fn(ctypes.byref(a), _stream(stream)))
+    return out
+
+
+def spec_verify_tokenwise(cu_drafts, draft_logits, target_logits, draft_tokens, temperature,
+                          kmax, seed, step, out=None, diag=False, stream=None):
+    """Token-by-token speculative sampling (see include/specverify.h)."""
+    return _verify(lib().spec_verify_tokenwise, cu_drafts, draft_logits, target_logits,
+                   draft_tokens, temperature, kmax, seed, step, out, diag, stream)
+
+
+def spec_verify_block(cu_drafts, draft_logits, target_logits, draft_tokens, temperature, kmax,
+                      seed, step, out=None, diag=False, stream=None):
+    """Block verification (see include/specverify.h)."""
+    return _verify(lib().spec_verify_block, cu_drafts, draft_logits, target_logits,
+                   draft_tokens, temperature, kmax, seed, step, out, diag, stream)
+
+
+def adaptive_pick_k(hidden, w, bias, verify_ms, mode=0, out=None, stream=None):
+    """Confidence head + pick k.  hidden [B, kmax, H], w [H] (float32/bf16, same dtype),
+    verify_ms [n_max + 1] float32.  Returns dict c [B, kmax], a [B, kmax], k [B], cu [B+1]."""
+    torch = _torch()
+    _dev(hidden, "hidden")
+    _dev(w, "w")
+    _dev(verify_ms, "verify_ms", torch.float32)
+    if w.dtype != hidden.dtype:
+        raise TypeError("hidden and w must share a dtype")
+    B, kmax, H = hidden.shape
+    if w.shape != (H,):
+        raise ValueError("w must be [H]")
+    dev = hidden.device
+    if out is None:
+        out = {"c": torch.empty((B, kmax), dtype=torch.float32, device=dev),
+               "a": torch.empty((B, kmax), dtype=torch.float32, device=dev),
+               "k": torch.empty(B, dtype=torch.int32, device=dev),
+               "cu": torch.empty(B + 1, dtype=torch.int32, device=dev)}
+    _check(lib().adaptive_pick_k(_ptr(hidden), _ptr(w), _dtype_code(hidden), float(bias), B, kmax,
+                                 H, _ptr(verify_ms), verify_ms.numel() - 1, int(mode),
+                                 _ptr(out["c"]), _ptr(out["a"]), _ptr(out["k"]), _ptr(out["cu"]),
+                                 _stream(stream)))
+    return out
+
+
+def spec_philox_uniforms(seed, step, n_streams, n_slots, device="cuda", stream=None):
+    """[n_streams, n_slots, 2] float64: (acceptance, sampling) uniforms of every (stream, slot)."""
+    torch = _torch()
+    out = torch.empty((n_streams, n_slots, 2), dtype=torch.float64, device=device)
+    _check(lib().spec_philox_uniforms(int(seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF,
+                                      n_streams, n_slots, _ptr(out), _stream(stream)))
+    return out

@@ -1,0 +1,174 @@
+// Device helpers shared by the verify, Markov-bias and pick-k kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/specverify.h"
+
+namespace sv {
+
+constexpr float kInf = __builtin_huge_valf();
+constexpr double kLog2e = 1.4426950408889634073599246810019;
+constexpr double kLn2 = 0.69314718055994530941723212145818;
+
+// ---------------------------------------------------------------------------------------
+// Scalar helpers
+// ---------------------------------------------------------------------------------------
+
+// 2^x on the special-function unit (relative error about 2^-22; subnormal results -> 0).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// max that returns NaN when either operand is NaN (so NaN rows are seen by the max alone).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// ---------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): counter (4 words), key (2 words).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    constexpr uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t hi0 = __umulhi(M0, c.x), lo0 = M0 * c.x;
+        const uint32_t hi1 = __umulhi(M1, c.z), lo1 = M1 * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+        k.x += W0;
+        k.y += W1;
+    }
+    return c;
+}
+
+// U(x) = ((x >> 8) + 0.5) * 2^-24, exact in double, strictly inside (0, 1).
+__device__ __forceinline__ double uniform24(uint32_t x) {
+    return ((double)(x >> 8) + 0.5) * 0x1p-24;
+}
+
+// (acceptance uniform, sampling uniform) of (stream, slot) in step `step` under `seed`.
+__device__ __forceinline__ double2 slot_uniforms(uint64_t seed, uint64_t step, uint32_t stream,
+                                                 uint32_t slot) {
+    const uint4 c = make_uint4(slot, stream, (uint32_t)step, (uint32_t)(step >> 32));
+    const uint2 k = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
+    const uint4 w = philox4x32_10(c, k);
+    return make_double2(uniform24(w.x), uniform24(w.y));
+}
+
+// ---------------------------------------------------------------------------------------
+// Warp reductions
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max_nan(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ int warp_min_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+// inclusive prefix sum across the warp (lane order)
+__device__ __forceinline__ double warp_incl_scan_d(double v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+// ---------------------------------------------------------------------------------------
+// Logit loaders: a "chunk" is E consecutive elements of one row.  E = 8 uses 16-byte loads
+// (one for bf16, two for float) and needs 16-byte aligned rows; E = 1 is the plain path.
+// ---------------------------------------------------------------------------------------
+template <typename T, int E>
+struct Chunk;
+
+template <>
+struct Chunk<__nv_bfloat16, 8> {
+    uint4 raw;
+    __device__ __forceinline__ void load(const void* row, int64_t chunk) {
+        raw = __ldg(reinterpret_cast<const uint4*>(row) + chunk);
+    }
+    __device__ __forceinline__ void unpack(float (&x)[8]) const {
+        x[0] = bf16_lo(raw.x); x[1] = bf16_hi(raw.x);
+        x[2] = bf16_lo(raw.y); x[3] = bf16_hi(raw.y);
+        x[4] = bf16_lo(raw.z); x[5] = bf16_hi(raw.z);
+        x[6] = bf16_lo(raw.w); x[7] = bf16_hi(raw.w);
+    }
+};
+
+template <>
+struct Chunk<float, 8> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const void* row, int64_t chunk) {
+        const float4* p = reinterpret_cast<const float4*>(row) + 2 * chunk;
+        a = __ldg(p);
+        b = __ldg(p + 1);
+    }
+    __device__ __forceinline__ void unpack(float (&x)[8]) const {
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+};
+
+template <>
+struct Chunk<__nv_bfloat16, 1> {
+    uint16_t raw;
+    __device__ __forceinline__ void load(const void* row, int64_t chunk) {
+        raw = __ldg(reinterpret_cast<const unsigned short*>(row) + chunk);
+    }
+    __device__ __forceinline__ void unpack(float (&x)[1]) const {
+        x[0] = __uint_as_float((uint32_t)raw << 16);
+    }
+};
+
+template <>
+struct Chunk<float, 1> {
+    float v;
+    __device__ __forceinline__ void load(const void* row, int64_t chunk) {
+        v = __ldg(reinterpret_cast<const float*>(row) + chunk);
+    }
+    __device__ __forceinline__ void unpack(float (&x)[1]) const { x[0] = v; }
+};
+
+// One element of a row (any alignment).
+template <typename T>
+__device__ __forceinline__ float load_elem(const void* row, int64_t i);
+template <>
+__device__ __forceinline__ float load_elem<float>(const void* row, int64_t i) {
+    return __ldg(reinterpret_cast<const float*>(row) + i);
+}
+template <>
+__device__ __forceinline__ float load_elem<__nv_bfloat16>(const void* row, int64_t i) {
+    return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(row) + i)
+                           << 16);
+}
+
+template <typename T>
+__device__ __forceinline__ const void* row_ptr(const void* base, int64_t row, int64_t V) {
+    return reinterpret_cast<const T*>(base) + row * V;
+}
+
+}  // namespace sv

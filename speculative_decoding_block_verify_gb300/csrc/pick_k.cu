@@ -1,0 +1,261 @@
+// Confidence head and adaptive verification (pick how many drafts to verify) on sm_103a.
+//
+// Method: "MTP Heads and Confidence Heads" (naphjohn.github.io), §7 (c_k = sigmoid(Linear(h))),
+// §9 (prefix survival a_j = c_1 ... c_j) and the figure text after §9 (the scheduler adds
+// candidates in descending a_j); "MTP, DSpark and Block Verification, Explained" (al-engr.com),
+// §6 (tokens per step = 1 + sum of a); "Teaching the Speculator What a Draft Costs"
+// (al-engr.com), "The controller, and the table it reads from" (best expected tokens per
+// millisecond, cost from verify_ms[num_tokens]).
+//
+// Kernel 1: one CTA per stream, one warp per draft slot: the dot h . w streams the hidden
+// state once (16-byte loads, float32 accumulation), then sigmoid, cumulative product and -
+// in per-stream mode - the stream's own pick, all in float64 scalars.
+// Kernel 2: one CTA: batch mode's ordering of all (stream, slot) entries and its pick, then
+// the exclusive prefix sum that gives cu_drafts.
+
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+#include "host_util.h"
+
+namespace sv {
+
+constexpr int kPickThreads = 1024;
+constexpr int kMaxBatchEntries = 4096;
+
+struct PickParams {
+    const void* hidden;
+    const void* w;
+    double bias;
+    int32_t B, kmax, H, mode, n_max;
+    const float* verify_ms;
+    float* c_out;
+    float* a_out;
+    int32_t* k_out;
+    int32_t* cu_out;
+    int64_t nchunk;
+};
+
+template <typename T, int E>
+__global__ void confidence_kernel(const PickParams p) {
+    __shared__ double c_s[SPEC_MAX_KMAX];
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int U = 4;
+    if (warp < p.kmax) {
+        const void* hrow = row_ptr<T>(p.hidden, (int64_t)b * p.kmax + warp, p.H);
+        float acc = 0.f;
+        for (int64_t base = 0; base < p.nchunk; base += 32 * U) {
+            Chunk<T, E> ch[U], cw[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t k = base + u * 32 + lane;
+                if (k < p.nchunk) {
+                    ch[u].load(hrow, k);
+                    cw[u].load(p.w, k);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t k = base + u * 32 + lane;
+                if (k < p.nchunk) {
+                    float xh[E], xw[E];
+                    ch[u].unpack(xh);
+                    cw[u].unpack(xw);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc = fmaf(xh[e], xw[e], acc);
+                }
+            }
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) {
+            const double x = (double)acc + p.bias;
+            c_s[warp] = (x >= 0.0) ? 1.0 / (1.0 + exp(-x)) : exp(x) / (1.0 + exp(x));
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double a = 1.0, e_n = 1.0;
+        int best_n = 0;
+        double best = 1.0 / (double)p.verify_ms[1];
+        for (int j = 0; j < p.kmax; ++j) {
+            a *= c_s[j];
+            p.c_out[(int64_t)b * p.kmax + j] = (float)c_s[j];
+            p.a_out[(int64_t)b * p.kmax + j] = (float)a;
+            e_n += a;                                   // E_{j+1}
+            const double ratio = e_n / (double)p.verify_ms[j + 2];
+            if (ratio > best) {
+                best = ratio;
+                best_n = j + 1;
+            }
+        }
+        if (p.mode == 0) p.k_out[b] = best_n;
+    }
+}
+
+// exclusive prefix sum of k over the batch (one CTA)
+__device__ void write_cu(const int32_t* k, int32_t* cu, int B) {
+    __shared__ int carry;
+    __shared__ int warp_tot[kPickThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < B; base += kPickThreads) {
+        const int i = base + tid;
+        int v = (i < B) ? k[i] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int wofs = 0;
+        for (int w = 0; w < warp; ++w) wofs += warp_tot[w];
+        if (i < B) cu[i] = carry + wofs + incl - v;
+        __syncthreads();
+        if (tid == kPickThreads - 1) carry += wofs + incl;
+        __syncthreads();
+    }
+    if (tid == 0) cu[B] = carry;
+}
+
+__global__ void __launch_bounds__(kPickThreads) pick_batch_kernel(const PickParams p) {
+    __shared__ float a_s[kMaxBatchEntries];
+    __shared__ uint16_t order[kMaxBatchEntries];   // order[rank] = entry
+    __shared__ int k_s[kMaxBatchEntries];
+    __shared__ double best_v[kPickThreads / 32];
+    __shared__ int best_m[kPickThreads / 32];
+    __shared__ double seg_tot[kPickThreads / 32];
+    __shared__ int m_star;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = p.B * p.kmax;
+    if (p.mode == 1) {
+        for (int e = tid; e < n; e += kPickThreads) a_s[e] = p.a_out[e];
+        for (int b = tid; b < p.B; b += kPickThreads) k_s[b] = 0;
+        __syncthreads();
+        // rank of entry e under (a desc, stream asc, slot asc); entry index = b * kmax + j
+        // already orders (stream, slot), so ties in a break by the entry index.
+        for (int e = tid; e < n; e += kPickThreads) {
+            const float ae = a_s[e];
+            int rank = 0;
+            for (int f = 0; f < n; ++f) {
+                const float af = a_s[f];
+                rank += (af > ae) || (af == ae && f < e);
+            }
+            order[rank] = e;
+        }
+        __syncthreads();
+        // S_m for m = 1..n: each thread owns a contiguous run of ranks
+        const int per = (n + kPickThreads - 1) / kPickThreads;
+        const int m0 = tid * per, m1 = min(n, m0 + per);
+        double run = 0.0;
+        for (int m = m0; m < m1; ++m) run += (double)a_s[order[m]];
+        // exclusive scan of the runs (warp, then block)
+        double incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double nb = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += nb;
+        }
+        if (lane == 31) seg_tot[warp] = incl;
+        __syncthreads();
+        double wofs = 0.0;
+        for (int w = 0; w < warp; ++w) wofs += seg_tot[w];
+        double s = wofs + incl - run;   // sum of the ranks before m0
+        // best ratio over this thread's m (m = number chosen, 1-based) ; m = 0 handled below
+        double bv = -1.0;
+        int bm = INT_MAX;
+        for (int m = m0; m < m1; ++m) {
+            s += (double)a_s[order[m]];
+            const double v = ((double)p.B + s) / (double)p.verify_ms[p.B + m + 1];
+            if (v > bv) { bv = v; bm = m + 1; }
+        }
+        if (tid == 0) {
+            const double v0 = (double)p.B / (double)p.verify_ms[p.B];
+            if (!(bv > v0)) { bv = v0; bm = 0; }   // ties go to the smaller m
+        }
+        // block argmax (larger value, then smaller m)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int om = __shfl_xor_sync(0xffffffffu, bm, o);
+            if (ov > bv || (ov == bv && om < bm)) { bv = ov; bm = om; }
+        }
+        if (lane == 0) { best_v[warp] = bv; best_m[warp] = bm; }
+        __syncthreads();
+        if (tid == 0) {
+            double v = best_v[0];
+            int m = best_m[0];
+            for (int w = 1; w < kPickThreads / 32; ++w)
+                if (best_v[w] > v || (best_v[w] == v && best_m[w] < m)) { v = best_v[w]; m = best_m[w]; }
+            m_star = m;
+        }
+        __syncthreads();
+        for (int r = tid; r < m_star; r += kPickThreads) atomicAdd(&k_s[order[r] / p.kmax], 1);
+        __syncthreads();
+        for (int b = tid; b < p.B; b += kPickThreads) p.k_out[b] = k_s[b];
+        __syncthreads();
+        write_cu(k_s, p.cu_out, p.B);
+    } else {
+        write_cu(p.k_out, p.cu_out, p.B);
+    }
+}
+
+template <typename T, int E>
+static cudaError_t launch_pick(const PickParams& p, cudaStream_t s) {
+    confidence_kernel<T, E><<<p.B, 32 * p.kmax, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    pick_batch_kernel<<<1, kPickThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace sv
+
+extern "C" int adaptive_pick_k(const void* hidden, const void* w, int32_t dtype, float bias,
+                               int32_t B, int32_t kmax, int32_t H, const float* verify_ms,
+                               int32_t n_max, int32_t mode, float* c_out, float* a_out,
+                               int32_t* k_out, int32_t* cu_drafts_out, void* stream) {
+    const char* name = "adaptive_pick_k";
+    if (mode != 0 && mode != 1) return sv::set_error(SPEC_ERR_ARG, "%s: mode must be 0 or 1", name);
+    if (!sv::valid_dtype(dtype))
+        return sv::set_error(SPEC_ERR_DTYPE, "%s: dtype must be SPEC_DTYPE_F32 or SPEC_DTYPE_BF16",
+                             name);
+    if (B < 1 || kmax < 1 || kmax > SPEC_MAX_KMAX || H < 1)
+        return sv::set_error(SPEC_ERR_SHAPE, "%s: B=%d kmax=%d H=%d out of range", name, B, kmax, H);
+    if (mode == 0 && n_max < kmax + 1)
+        return sv::set_error(SPEC_ERR_SHAPE, "%s: verify_ms needs n_max >= kmax + 1", name);
+    if (mode == 1 && ((int64_t)B * (kmax + 1) > n_max || (int64_t)B * kmax > sv::kMaxBatchEntries))
+        return sv::set_error(SPEC_ERR_SHAPE,
+                             "%s: batch mode needs n_max >= B*(kmax+1) and B*kmax <= %d", name,
+                             sv::kMaxBatchEntries);
+    if (!hidden || !w || !verify_ms || !c_out || !a_out || !k_out || !cu_drafts_out)
+        return sv::set_error(SPEC_ERR_ARG, "%s: a pointer is NULL", name);
+    sv::PickParams p;
+    p.hidden = hidden;
+    p.w = w;
+    p.bias = (double)bias;
+    p.B = B;
+    p.kmax = kmax;
+    p.H = H;
+    p.mode = mode;
+    p.n_max = n_max;
+    p.verify_ms = verify_ms;
+    p.c_out = c_out;
+    p.a_out = a_out;
+    p.k_out = k_out;
+    p.cu_out = cu_drafts_out;
+    const bool aligned = (H % 8 == 0) && ((uintptr_t)hidden % 16 == 0) && ((uintptr_t)w % 16 == 0);
+    p.nchunk = aligned ? H / 8 : H;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (dtype == SPEC_DTYPE_BF16)
+        e = aligned ? sv::launch_pick<__nv_bfloat16, 8>(p, s) : sv::launch_pick<__nv_bfloat16, 1>(p, s);
+    else
+        e = aligned ? sv::launch_pick<float, 8>(p, s) : sv::launch_pick<float, 1>(p, s);
+    if (e != cudaSuccess) return sv::set_cuda_error(e, name);
+    return sv::clear_error();
+}
