@@ -238,7 +238,7 @@ def _block(res, ps, qs, xs, log_rho, seed, step, stream):
     for i in range(n + 1):
         diag[i, D_W] = w[i]
     r = [float("nan")] * (n + 1)
-    for i in range(1, n):
+    for i in range(0, n):
         r[i] = float(np.sum(residual_weights(w[i], np.exp(ps[i]), np.exp(qs[i]))))
         diag[i, D_R] = r[i]
     h = block_h(w, r)
@@ -255,8 +255,6 @@ def _block(res, ps, qs, xs, log_rho, seed, step, stream):
     if tau == n:
         return _finish(res, tau, xs, np.exp(ps[n]), us)
     wts = residual_weights(w[tau], np.exp(ps[tau]), np.exp(qs[tau]))
-    if tau == 0:
-        diag[0, D_R] = float(np.sum(wts))
     return _finish(res, tau, xs, wts, us)
 
 
