@@ -166,6 +166,18 @@ int spec_verify_tokenwise(const spec_verify_args* args, void* stream);
 int spec_verify_block(const spec_verify_args* args, void* stream);
 
 /*
+ * spec_verify_launch_info - the launch configuration a verify call with these arguments
+ * would use (no launch, no device data read; only the scalar fields and the two logit
+ * pointers' alignment are examined).  cluster_size: CTAs per stream; resident_clusters: how
+ * many such clusters the current device holds at once; elems_per_load: 8 when the rows take
+ * the 16-byte vector path, 1 otherwise.
+ * Errors: as spec_verify_tokenwise (without the NULL checks of the tensor pointers), and
+ * SPEC_ERR_ARG when an output pointer is NULL.
+ */
+int spec_verify_launch_info(const spec_verify_args* args, int32_t* cluster_size,
+                            int32_t* resident_clusters, int32_t* elems_per_load);
+
+/*
  * adaptive_pick_k - confidence head and adaptive verification.
  * [P2] §7 "Only Then Comes the Confidence Head": c_k = sigmoid(h_k . w + bias);
  * §9 "Why It Is Called Prefix Survival Probability": a_j = c_1 ... c_j;

@@ -22,7 +22,7 @@ import os
 
 __all__ = [
     "dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block", "adaptive_pick_k",
-    "spec_philox_uniforms", "lib", "lib_path", "SpecError",
+    "spec_philox_uniforms", "spec_verify_launch_info", "lib", "lib_path", "SpecError",
     "DTYPE_F32", "DTYPE_BF16", "STATUS_NAMES", "DIAG_COLS",
 ]
 
@@ -32,7 +32,8 @@ DIAG_COLS = 8
 STATUS_NAMES = {0: "OK", 1: "BAD_TEMPERATURE", 2: "BAD_TOKEN", 3: "BAD_ROW",
                 4: "ZERO_DRAFT_PROB", 5: "BAD_OFFSETS", 6: "TIMEOUT", 7: "NUMERIC"}
 EXPORTED = ["dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block",
-            "adaptive_pick_k", "spec_philox_uniforms", "spec_last_error", "spec_version"]
+            "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info",
+            "spec_last_error", "spec_version"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -82,10 +83,12 @@ def lib():
     L.adaptive_pick_k.argtypes = [vp, vp, i32, ctypes.c_float, i32, i32, i32, vp, i32, i32,
                                   vp, vp, vp, vp, vp]
     L.spec_philox_uniforms.argtypes = [u64, u64, i32, i32, vp, vp]
+    L.spec_verify_launch_info.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.POINTER(i32),
+                                          ctypes.POINTER(i32), ctypes.POINTER(i32)]
     L.spec_last_error.restype = ctypes.c_char_p
     L.spec_version.restype = ctypes.c_int32
     for name in ("dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block",
-                 "adaptive_pick_k", "spec_philox_uniforms"):
+                 "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -239,6 +242,19 @@ def adaptive_pick_k(hidden, w, bias, verify_ms, mode=0, out=None, stream=None):
                                  _ptr(out["c"]), _ptr(out["a"]), _ptr(out["k"]), _ptr(out["cu"]),
                                  _stream(stream)))
     return out
+
+
+def spec_verify_launch_info(B, V, kmax, draft_dtype=DTYPE_BF16, target_dtype=DTYPE_BF16,
+                            aligned=True):
+    """(cluster_size, resident_clusters, elems_per_load) a verify call of this shape uses."""
+    a = VerifyArgs()
+    a.B, a.V, a.kmax = B, V, kmax
+    a.draft_dtype, a.target_dtype = draft_dtype, target_dtype
+    a.draft_logits = a.target_logits = 0 if aligned else 2
+    c, r, e = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().spec_verify_launch_info(ctypes.byref(a), ctypes.byref(c), ctypes.byref(r),
+                                         ctypes.byref(e)))
+    return c.value, r.value, e.value
 
 
 def spec_philox_uniforms(seed, step, n_streams, n_slots, device="cuda", stream=None):

@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/specverify.h"
+#include "specverify.h"
 
 namespace sv {
 
@@ -71,6 +71,11 @@ __device__ __forceinline__ double2 slot_uniforms(uint64_t seed, uint64_t step, u
 __device__ __forceinline__ float warp_max_nan(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
 __device__ __forceinline__ float warp_sum(float v) {
@@ -169,6 +174,34 @@ __device__ __forceinline__ float load_elem<__nv_bfloat16>(const void* row, int64
 template <typename T>
 __device__ __forceinline__ const void* row_ptr(const void* base, int64_t row, int64_t V) {
     return reinterpret_cast<const T*>(base) + row * V;
+}
+
+}  // namespace sv
+
+namespace sv {
+
+// ---------------------------------------------------------------------------------------
+// Packed float32x2 arithmetic (one instruction for two lanes of data)
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long f2_pack(float2 a) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long r) {
+    float2 a;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+    return a;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)), "l"(f2_pack(c)));
+    return f2_unpack(d);
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+    return f2_unpack(d);
 }
 
 }  // namespace sv

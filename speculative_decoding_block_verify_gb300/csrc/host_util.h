@@ -6,7 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 
-#include "../../include/specverify.h"
+#include "specverify.h"
 
 namespace sv {
 

@@ -8,19 +8,26 @@
 //   * one thread-block cluster of C CTAs per stream; CTA c owns a contiguous vocabulary slice
 //     of every row of its stream, split into one contiguous segment per warp (C x 8 segments
 //     per row, in vocabulary order);
-//   * stats sweep: every logit of the stream is read from HBM exactly once (16-byte loads);
-//     each lane keeps an online (max, sum 2^((l - max) a), argmax) per row, a = log2(e) / T;
-//     warps publish per-segment partials in shared memory;
+//   * stats sweep: every logit of the stream is read from HBM exactly once, 16-byte cp.async
+//     copies into a per-warp shared-memory ring; each lane keeps, per row, s = sum 2^(l a - K)
+//     against an integer reference K (a = log2(e)/T carried as a_hi + a_lo, so every exponent
+//     is two FMAs with one rounding and the temperature is exact to ~1e-14).  The fast path
+//     has no branch per element; a chunk that would overflow the running sum (or holds a NaN)
+//     takes an exact slow path that raises K;
 //   * one cluster barrier, then every CTA reduces all partials through distributed shared
 //     memory in the same order, so every CTA holds bit-identical row statistics and takes the
-//     same per-stream decisions (float64 scalars) without further communication;
-//   * block verification evaluates tau top-down (i = N .. 1): h_N = w_N needs no sweep; an i
-//     with eta_i > w_i fails without one (h_i <= w_i); otherwise a residual sweep of slot i
-//     (re-read, mostly from L2) gives r_i and h_i; tau = 0 needs one sweep of slot 0;
-//   * the draw: per-segment masses give a coarse CDF; the warp whose segment holds U*R
-//     rescans that segment and writes the token.
-// Slot 0 is the last pair read by the stats sweep so that its residual sweep (the common
-// tau = 0 case at low acceptance) finds it in L2.
+//     same per-stream decisions without further communication; the per-stream scalars (rho,
+//     the running product w, h) are double-float on the float32 pipes;
+//   * block verification: h_N = w_N needs no residual; slot i < N is a candidate only if
+//     eta_i <= w_i (since h_i <= w_i); the residual masses of all candidates and of slot 0 are
+//     computed in one cluster-wide sweep (re-read, mostly from L2), then tau = the largest
+//     candidate with eta_i <= h_i, else 0.  The token-wise rule needs one residual (at tau);
+//   * the draw: a 64-bit fixed-point CDF over the segments (exact integer prefix sums), then
+//     the warp whose segment holds U*R rescans it in the same fixed point and writes the
+//     token.  CTAs arrive at the final cluster barrier as soon as their last distributed-
+//     shared-memory read is done, so none waits for the rescan.
+// Slot 0 is the last pair read by the stats sweep so that its residual (the common tau = 0
+// case at low acceptance) finds it in L2.
 
 #include <cooperative_groups.h>
 
@@ -28,6 +35,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "df.cuh"
 #include "host_util.h"
 
 namespace cg = cooperative_groups;
@@ -39,6 +47,8 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 8;
 constexpr int kMaxRows = 2 * SPEC_MAX_KMAX + 1;
 constexpr int kMaxSeg = kMaxCluster * kWarps;
+constexpr int kRingBytesPerCta = 48 * 1024;
+constexpr float kNoRef = -1e30f;     // reference of a lane that has seen no finite logit
 
 struct VerifyParams {
     int32_t B, V, kmax, rule;
@@ -53,207 +63,349 @@ struct VerifyParams {
     int32_t* n_emit;
     int32_t* status;
     float* diag;
-    int64_t nchunk;      // chunks per row
+    int64_t nchunk;      // chunks of 8 (or 1) elements per row
     int64_t seg_chunks;  // chunks per warp segment
 };
 
+// Per-warp partial of one row.  T > 0: K = integer reference, (s_hi, s_lo) = sum 2^(l a - K).
+// T = 0: K = the segment maximum, idx = its lowest index.
 struct Part {
-    float m;
-    float s;
+    float K;
+    float s_hi, s_lo;
     int idx;
 };
 
 struct Shared {
     Part part[kMaxRows][kWarps];
-    float res_part[2][kWarps];
-    float row_m[kMaxRows];
-    double row_z[kMaxRows];
-    int row_arg[kMaxRows];
-    double seg_w[kMaxSeg];
-    double bonus_w[kMaxSeg];
-    double log2px[SPEC_MAX_KMAX];
-    double log2qx[SPEC_MAX_KMAX];
-    double rho[SPEC_MAX_KMAX];
-    double log2w[SPEC_MAX_KMAX + 1];
-    double w[SPEC_MAX_KMAX + 1];
-    double h[SPEC_MAX_KMAX + 1];
-    double r[SPEC_MAX_KMAX + 1];
-    double u_acc[SPEC_MAX_KMAX + 1];
-    double u_smp[SPEC_MAX_KMAX + 1];
-    double resid_R;
-    double sample_t;
+    float res_part[SPEC_MAX_KMAX + 1][kWarps];
+    float rowK[kMaxRows];
+    df rowZ[kMaxRows];
+    int rowArg[kMaxRows];
+    float bonus_w[kMaxSeg];
+    df rho[SPEC_MAX_KMAX];
+    df w[SPEC_MAX_KMAX + 1];
+    df h[SPEC_MAX_KMAX + 1];
+    df r[SPEC_MAX_KMAX + 1];
+    df u_acc[SPEC_MAX_KMAX + 1];
+    uint32_t u_smp[SPEC_MAX_KMAX + 1];
+    float cval[SPEC_MAX_KMAX + 1];     // residual weight scale w_i Z_q / Z_p per slot
+    float lq[SPEC_MAX_KMAX], lp[SPEC_MAX_KMAX];
     int x[SPEC_MAX_KMAX];
-    int N, status, greedy, tau, pass_slot, done, sample_seg, sample_bonus;
-    float a;
-    float cc;
+    int pass_list[SPEC_MAX_KMAX + 1];
+    int n_pass;
+    int N, status, greedy, tau, sample_seg, sample_bonus;
+    unsigned long long sample_t;   // in-segment target (fixed point)
+    float sample_scale;            // fixed-point scale of the draw's weights
+    float a_hi, a_lo;
 };
 
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    cluster_arrive();
+    cluster_wait();
 }
 
-template <typename T, int E>
-struct Unroll {
-    static constexpr int value = (E == 1) ? 8 : (sizeof(T) == 2 ? 4 : 2);
+// ---------------------------------------------------------------------------------------
+// cp.async helpers
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------------------------------
+// Chunk feeds.  A stage is U chunks per lane of up to two rows (q and p): lane L of a warp
+// takes chunks k0 + u*32 + L, u < U.  The vector path (E = 8, 16-byte aligned rows) stages
+// through a per-warp cp.async ring of D stages; the plain path (E = 1) loads directly.
+// Each lane reads back only the bytes it copied, so the ring needs no barrier.
+// ---------------------------------------------------------------------------------------
+template <typename DQ, typename DP, int E>
+struct Feed;
+
+template <typename DQ, typename DP>
+struct Feed<DQ, DP, 8> {
+    static constexpr int BQ = 8 * (int)sizeof(DQ);
+    static constexpr int BP = 8 * (int)sizeof(DP);
+    static constexpr int U = (BQ + BP) <= 32 ? 2 : 1;
+    static constexpr int SUB = 32 * (BQ + BP);               // one chunk of each row, 32 lanes
+    static constexpr int STAGE = U * SUB;
+    static constexpr int D = (kRingBytesPerCta / kWarps / STAGE) < 2 ? 2 : (kRingBytesPerCta / kWarps / STAGE);
+    static constexpr int RING = D * STAGE;                   // bytes per warp
+    char* base;
+    int lane;
+    __device__ __forceinline__ void issue(int slot, const void* rq, const void* rp, int64_t k0, int64_t c1) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = k0 + u * 32 + lane;
+            if (k < c1) {
+                char* sq = base + slot * STAGE + u * SUB + lane * BQ;
+                char* sp = base + slot * STAGE + u * SUB + 32 * BQ + lane * BP;
+                if (rq) {
+                    const char* g = reinterpret_cast<const char*>(rq) + k * BQ;
+#pragma unroll
+                    for (int v = 0; v < BQ / 16; ++v) cp_async16(sq + 16 * v, g + 16 * v);
+                }
+                const char* g = reinterpret_cast<const char*>(rp) + k * BP;
+#pragma unroll
+                for (int v = 0; v < BP / 16; ++v) cp_async16(sp + 16 * v, g + 16 * v);
+            }
+        }
+        cp_async_commit();
+    }
+    __device__ __forceinline__ void empty() { cp_async_commit(); }
+    __device__ __forceinline__ void wait() { cp_async_wait<D - 1>(); }
+    __device__ __forceinline__ void drain() { cp_async_wait<0>(); }
+    __device__ __forceinline__ void get(int slot, int u, const void*, const void*, int64_t, bool has_q,
+                                        float (&xq)[8], float (&xp)[8]) const {
+        const char* sq = base + slot * STAGE + u * SUB + lane * BQ;
+        const char* sp = base + slot * STAGE + u * SUB + 32 * BQ + lane * BP;
+        if (has_q) unpack<DQ>(sq, xq);
+        unpack<DP>(sp, xp);
+    }
+    template <typename T>
+    __device__ __forceinline__ static void unpack(const char* s, float (&x)[8]) {
+        if (sizeof(T) == 2) {
+            const uint4 v = *reinterpret_cast<const uint4*>(s);
+            x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+            x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+        } else {
+            const float4 a = *reinterpret_cast<const float4*>(s);
+            const float4 b = *reinterpret_cast<const float4*>(s + 16);
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+            x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        }
+    }
+};
+
+template <typename DQ, typename DP>
+struct Feed<DQ, DP, 1> {
+    static constexpr int U = 4;
+    static constexpr int D = 1;
+    static constexpr int RING = 0;
+    char* base;
+    int lane;
+    __device__ __forceinline__ void issue(int, const void*, const void*, int64_t, int64_t) {}
+    __device__ __forceinline__ void empty() {}
+    __device__ __forceinline__ void wait() {}
+    __device__ __forceinline__ void drain() {}
+    __device__ __forceinline__ void get(int, int, const void* rq, const void* rp, int64_t k, bool has_q,
+                                        float (&xq)[1], float (&xp)[1]) const {
+        if (has_q) xq[0] = load_elem<DQ>(rq, k);
+        xp[0] = load_elem<DP>(rp, k);
+    }
 };
 
 // ---------------------------------------------------------------------------------------
-// Per-lane online row statistics
+// Per-lane accumulators
 // ---------------------------------------------------------------------------------------
-template <int E, bool ARG, bool SUM>
-struct LaneAcc {
+// Pairwise sum of a chunk's E terms (each term takes part in log2(E) roundings).
+template <int E>
+__device__ __forceinline__ float chunk_sum(const float (&t)[E]) {
+    if constexpr (E == 1) {
+        return t[0];
+    } else {
+        float2 v[E / 2];
+#pragma unroll
+        for (int j = 0; j < E / 2; ++j) v[j] = make_float2(t[2 * j], t[2 * j + 1]);
+#pragma unroll
+        for (int w = E / 2; w > 1; w /= 2)
+#pragma unroll
+            for (int j = 0; j < w / 2; ++j) v[j] = fadd2(v[j], v[j + w / 2]);
+        return v[0].x + v[0].y;
+    }
+}
+
+// Kahan-compensated running sum of chunk sums: the true sum is s - c.  Accumulating one
+// float per chunk against a large running total would otherwise lose ~3e-8 of the total per
+// addition when one token dominates the row.
+struct Kahan {
+    float s = 0.f, c = 0.f;
+    __device__ __forceinline__ void add(float t) {
+        const float y = __fsub_rn(t, c);
+        const float u = __fadd_rn(s, y);
+        c = __fsub_rn(__fsub_rn(u, s), y);
+        s = u;
+    }
+    __device__ __forceinline__ df value() const { return fast_two_sum(s, -c); }
+    __device__ __forceinline__ void scale(float f) {
+        s *= f;
+        c *= f;
+    }
+};
+
+// sum 2^(x a - K) of one lane (T > 0 rows), with the reference K raised only when needed
+template <int E>
+struct LaneSum {
+    float K = kNoRef;
+    Kahan acc;
+
+    __device__ __forceinline__ float terms(const float (&x)[E], float ah, float al) const {
+        float t[E];
+        if (E == 1) {
+            t[0] = ex2(fmaf(x[0], al, fmaf(x[0], ah, -K)));
+        } else {
+            const float2 nk = make_float2(-K, -K), a2h = make_float2(ah, ah), a2l = make_float2(al, al);
+#pragma unroll
+            for (int j = 0; j < E / 2; ++j) {
+                const float2 xx = make_float2(x[2 * j], x[2 * j + 1]);
+                const float2 e = ffma2(xx, a2l, ffma2(xx, a2h, nk));
+                t[2 * j] = ex2(e.x);
+                t[2 * j + 1] = ex2(e.y);
+            }
+        }
+        return chunk_sum<E>(t);
+    }
+    // The fast path keeps every term of the chunk <= 16, i.e. its exponent x a - K <= 4, where
+    // float32 rounds the exponent to 1.2e-7 (2^e to ~8e-8); a chunk with a larger sum (a new
+    // maximum more than 4 above K, the first finite chunk, +inf or NaN) raises K to
+    // ceil(max x a) and is recomputed.
+    __device__ __forceinline__ void add(const float (&x)[E], float ah, float al) {
+        const float t = terms(x, ah, al);
+        if (t <= 16.f) {
+            acc.add(t);
+            return;
+        }
+        float vm = x[0];
+#pragma unroll
+        for (int j = 1; j < E; ++j) vm = fmaxf(vm, x[j]);   // NaN-ignoring
+        const float kv = ceilf(vm * ah);
+        if (kv > K) {
+            acc.scale(pow2_int(K - kv));
+            K = kv;
+        }
+        acc.add(terms(x, ah, al));                             // NaN / inf stay and poison the row
+    }
+    // warp-combine and publish (lane 0)
+    __device__ __forceinline__ void publish(Part* dst, int lane) const {
+        const float Kw = warp_max(K);
+        df sum = df_scale(acc.value(), K == Kw ? 1.f : pow2_int(K - Kw));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const df other{__shfl_xor_sync(0xffffffffu, sum.hi, o), __shfl_xor_sync(0xffffffffu, sum.lo, o)};
+            sum = df_add(sum, other);
+        }
+        if (lane == 0) *dst = Part{Kw, sum.hi, sum.lo, INT_MAX};
+    }
+};
+
+// max and its lowest index (T = 0 rows); NaN propagates
+template <int E>
+struct LaneMax {
     float m = -kInf;
-    float s = 0.f;
     int idx = INT_MAX;
-    __device__ __forceinline__ void add(const float (&x)[E], int64_t elem0, float a) {
+    __device__ __forceinline__ void add(const float (&x)[E], int64_t elem0) {
         float vm = x[0];
 #pragma unroll
         for (int j = 1; j < E; ++j) vm = fmax_nan(vm, x[j]);
-        if (!(vm <= m)) {  // a new maximum (or a NaN)
-            if (ARG) {
-                int j0 = 0;
+        if (!(vm <= m)) {
+            int j0 = 0;
 #pragma unroll
-                for (int j = E - 1; j >= 0; --j)
-                    if (x[j] == vm) j0 = j;
-                idx = (int)(elem0 + j0);
-            }
-            if (SUM) s = (m == -kInf) ? 0.f : s * ex2((m - vm) * a);
+            for (int j = E - 1; j >= 0; --j)
+                if (x[j] == vm) j0 = j;
+            idx = (int)(elem0 + j0);
             m = fmax_nan(m, vm);
         }
-        if (SUM && m != -kInf) {
-#pragma unroll
-            for (int j = 0; j < E; ++j) s += ex2((x[j] - m) * a);
-        }
     }
-    // warp-combine and publish (lane 0)
-    __device__ __forceinline__ void publish(Part* dst, float a, int lane) const {
+    __device__ __forceinline__ void publish(Part* dst, int lane) const {
         const float mw = warp_max_nan(m);
-        float sw = 0.f;
-        if (SUM) sw = warp_sum((m == -kInf) ? 0.f : s * ex2((m - mw) * a));
-        const int iw = ARG ? warp_min_i((m == mw) ? idx : INT_MAX) : INT_MAX;
-        if (lane == 0) *dst = Part{mw, sw, iw};
+        const int iw = warp_min_i((m == mw) ? idx : INT_MAX);
+        if (lane == 0) *dst = Part{mw, 0.f, 0.f, iw};
     }
 };
 
-// stats of one row pair (draft row q, target row p) over this warp's segment [c0, c1)
-template <typename DQ, typename DP, int E>
-__device__ __forceinline__ void stats_pair(const void* rq, const void* rp, int64_t c0, int64_t c1,
-                                           float a, int lane, Part* dq, Part* dp) {
-    constexpr int U = Unroll<DQ, E>::value < Unroll<DP, E>::value ? Unroll<DQ, E>::value
-                                                                 : Unroll<DP, E>::value;
-    LaneAcc<E, false, true> aq;
-    LaneAcc<E, true, true> ap;
-    for (int64_t base = c0; base < c1; base += 32 * U) {
-        Chunk<DQ, E> cq[U];
-        Chunk<DP, E> cp[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t k = base + u * 32 + lane;
-            if (k < c1) {
-                cq[u].load(rq, k);
-                cp[u].load(rp, k);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t k = base + u * 32 + lane;
-            if (k < c1) {
-                float x[E];
-                cq[u].unpack(x);
-                aq.add(x, k * E, a);
-                cp[u].unpack(x);
-                ap.add(x, k * E, a);
-            }
-        }
-    }
-    aq.publish(dq, a, lane);
-    ap.publish(dp, a, lane);
-}
-
-// stats of one target row (bonus row: with sums; greedy rows: max/argmax only)
-template <typename DP, int E, bool SUM>
-__device__ __forceinline__ void stats_single(const void* rp, int64_t c0, int64_t c1, float a,
-                                             int lane, Part* dp) {
-    constexpr int U = 2 * Unroll<DP, E>::value;
-    LaneAcc<E, true, SUM> ap;
-    for (int64_t base = c0; base < c1; base += 32 * U) {
-        Chunk<DP, E> cp[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t k = base + u * 32 + lane;
-            if (k < c1) cp[u].load(rp, k);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t k = base + u * 32 + lane;
-            if (k < c1) {
-                float x[E];
-                cp[u].unpack(x);
-                ap.add(x, k * E, a);
-            }
-        }
-    }
-    ap.publish(dp, a, lane);
-}
-
-// residual weights max(0, cc * 2^((lp - mp) a) - 2^((lq - mq) a)) of one chunk
+// residual weights max(0, c 2^(xp a - Kp) - 2^(xq a - Kq)) of one chunk
 template <int E>
-__device__ __forceinline__ void residual_weights(const float (&xq)[E], const float (&xp)[E],
-                                                 float mq, float mp, float a, float cc,
-                                                 float (&wt)[E]) {
+__device__ __forceinline__ void resid_weights(const float (&xq)[E], const float (&xp)[E], float Kq, float Kp,
+                                              float ah, float al, float c, float (&w)[E]) {
+    if (E == 1) {
+        const float ep = ex2(fmaf(xp[0], al, fmaf(xp[0], ah, -Kp)));
+        const float eq = ex2(fmaf(xq[0], al, fmaf(xq[0], ah, -Kq)));
+        w[0] = fmaxf(0.f, fmaf(c, ep, -eq));
+    } else {
+        const float2 a2h = make_float2(ah, ah), a2l = make_float2(al, al);
+        const float2 nkp = make_float2(-Kp, -Kp), nkq = make_float2(-Kq, -Kq);
 #pragma unroll
-    for (int j = 0; j < E; ++j) {
-        const float ep = ex2((xp[j] - mp) * a);
-        const float eq = ex2((xq[j] - mq) * a);
-        wt[j] = fmaxf(0.f, fmaf(cc, ep, -eq));
+        for (int j = 0; j < E / 2; ++j) {
+            const float2 pp = make_float2(xp[2 * j], xp[2 * j + 1]);
+            const float2 qq = make_float2(xq[2 * j], xq[2 * j + 1]);
+            const float2 e1 = ffma2(pp, a2l, ffma2(pp, a2h, nkp));
+            const float2 e2 = ffma2(qq, a2l, ffma2(qq, a2h, nkq));
+            w[2 * j] = fmaxf(0.f, fmaf(c, ex2(e1.x), -ex2(e2.x)));
+            w[2 * j + 1] = fmaxf(0.f, fmaf(c, ex2(e1.y), -ex2(e2.y)));
+        }
     }
 }
 
-// sum of residual weights over this warp's segment
-template <typename DQ, typename DP, int E>
-__device__ __forceinline__ float residual_sum(const void* rq, const void* rp, int64_t c0,
-                                              int64_t c1, float mq, float mp, float a, float cc,
-                                              int lane) {
-    constexpr int U = Unroll<DQ, E>::value < Unroll<DP, E>::value ? Unroll<DQ, E>::value
-                                                                 : Unroll<DP, E>::value;
-    float s = 0.f;
-    for (int64_t base = c0; base < c1; base += 32 * U) {
-        Chunk<DQ, E> cq[U];
-        Chunk<DP, E> cp[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t k = base + u * 32 + lane;
-            if (k < c1) {
-                cq[u].load(rq, k);
-                cp[u].load(rp, k);
-            }
+// ---------------------------------------------------------------------------------------
+// Warp sweep over this warp's segment [c0, c1) of a list of items (a row or a row pair),
+// each split into groups of U * 32 chunks; the ring runs D - 1 groups ahead of the consumer.
+// rows(it, rq, rp) gives an item's rows; begin(it) / consume(k, xq, xp) / end(it) see the
+// items in order.
+// ---------------------------------------------------------------------------------------
+template <typename DQ, typename DP, int E, typename RowsFn, typename BeginFn, typename ConsumeFn, typename EndFn>
+__device__ __forceinline__ void sweep(Feed<DQ, DP, E>& feed, int items, int64_t c0, int64_t c1, int lane,
+                                      RowsFn rows, BeginFn begin_item, ConsumeFn consume, EndFn end_item) {
+    constexpr int D = Feed<DQ, DP, E>::D;
+    constexpr int U = Feed<DQ, DP, E>::U;
+    const int G = (c1 > c0) ? (int)((c1 - c0 + 32 * U - 1) / (32 * U)) : 0;
+    int ii = 0, gi = 0, slot_i = 0;
+    const void *iq = nullptr, *ip = nullptr;
+    if (G > 0 && items > 0) rows(0, iq, ip);
+    auto issue_next = [&]() {
+        if (ii < items) feed.issue(slot_i, iq, ip, c0 + (int64_t)gi * 32 * U, c1);
+        else feed.empty();
+        if (++slot_i == D) slot_i = 0;
+        if (++gi == G) {
+            gi = 0;
+            ++ii;
+            if (ii < items) rows(ii, iq, ip);
         }
+    };
+    if (G > 0)
+        for (int s = 0; s < D - 1; ++s) issue_next();
+    int slot_c = 0;
+    for (int it = 0; it < items; ++it) {
+        const void *cq, *cp;
+        rows(it, cq, cp);
+        begin_item(it);
+        for (int g = 0; g < G; ++g) {
+            issue_next();
+            feed.wait();
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t k = base + u * 32 + lane;
-            if (k < c1) {
-                float xq[E], xp[E], wt[E];
-                cq[u].unpack(xq);
-                cp[u].unpack(xp);
-                residual_weights<E>(xq, xp, mq, mp, a, cc, wt);
-#pragma unroll
-                for (int j = 0; j < E; ++j) s += wt[j];
+            for (int u = 0; u < U; ++u) {
+                const int64_t k = c0 + ((int64_t)g * U + u) * 32 + lane;
+                if (k < c1) {
+                    float xq[E], xp[E];
+                    feed.get(slot_c, u, cq, cp, k, cq != nullptr, xq, xp);
+                    consume(k, xq, xp);
+                }
             }
+            if (++slot_c == D) slot_c = 0;
         }
+        end_item(it);
     }
-    return warp_sum(s);
+    feed.drain();
 }
 
-// Inverse-CDF rescan of one warp segment: the smallest element whose running mass reaches t
-// (or, if rounding keeps the running mass below t, the segment's last positive element).
+// Inverse-CDF rescan of one warp segment in 64-bit fixed point (weights times `scale`): the
+// first element whose running sum exceeds t, or - if rounding keeps the segment's sum at or
+// below t - the segment's last positive element.
 template <typename DQ, typename DP, int E, bool BONUS>
-__device__ __forceinline__ int rescan_segment(const void* rq, const void* rp, int64_t c0,
-                                              int64_t c1, float mq, float mp, float a, float cc,
-                                              double t, int lane) {
-    constexpr int U = Unroll<DQ, E>::value < Unroll<DP, E>::value ? Unroll<DQ, E>::value
-                                                                 : Unroll<DP, E>::value;
-    double run = 0.0;
+__device__ __forceinline__ int rescan_segment(const void* rq, const void* rp, int64_t c0, int64_t c1,
+                                              float Kq, float Kp, float ah, float al, float c, float scale,
+                                              unsigned long long t, int lane) {
+    constexpr int U = 4;
+    unsigned long long run = 0;
     int y = -1, ylast = -1;
     for (int64_t base = c0; base < c1 && y < 0; base += 32 * U) {
         Chunk<DQ, E> cq[U];
@@ -269,44 +421,49 @@ __device__ __forceinline__ int rescan_segment(const void* rq, const void* rp, in
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t k = base + u * 32 + lane;
-            float wt[E];
-            float lsum = 0.f;
+            unsigned long long qv[E];
+            unsigned long long lsum = 0;
             int lpos = -1;
             if (k < c1) {
-                float xp[E];
+                float xp[E], w[E];
                 cp[u].unpack(xp);
                 if (BONUS) {
 #pragma unroll
-                    for (int j = 0; j < E; ++j) wt[j] = ex2((xp[j] - mp) * a);
+                    for (int j = 0; j < E; ++j) w[j] = ex2(fmaf(xp[j], al, fmaf(xp[j], ah, -Kp)));
                 } else {
                     float xq[E];
                     cq[u].unpack(xq);
-                    residual_weights<E>(xq, xp, mq, mp, a, cc, wt);
+                    resid_weights<E>(xq, xp, Kq, Kp, ah, al, c, w);
                 }
 #pragma unroll
                 for (int j = 0; j < E; ++j) {
-                    lsum += wt[j];
-                    if (wt[j] > 0.f) lpos = (int)(k * E + j);
+                    qv[j] = __float2ull_rn(w[j] * scale);
+                    lsum += qv[j];
+                    if (qv[j] > 0) lpos = (int)(k * E + j);
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < E; ++j) wt[j] = 0.f;
+                for (int j = 0; j < E; ++j) qv[j] = 0;
             }
-            const double incl = warp_incl_scan_d((double)lsum, lane);
-            const double total = __shfl_sync(0xffffffffu, incl, 31);
-            const unsigned hit = __ballot_sync(0xffffffffu, lsum > 0.f && run + incl >= t);
-            // last positive element so far (the fallback)
+            unsigned long long incl = lsum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
+            const unsigned hit = __ballot_sync(0xffffffffu, lsum > 0 && run + incl > t);
             const int lp_max = __reduce_max_sync(0xffffffffu, lpos);
             if (lp_max >= 0) ylast = lp_max;
             if (hit && y < 0) {
                 const int L = __ffs(hit) - 1;
                 int yl = -1;
                 if (lane == L) {
-                    double acc = run + incl - (double)lsum;
+                    unsigned long long acc = run + incl - lsum;
 #pragma unroll
                     for (int j = 0; j < E; ++j) {
-                        acc += (double)wt[j];
-                        if (yl < 0 && wt[j] > 0.f && acc >= t) yl = (int)(k * E + j);
+                        acc += qv[j];
+                        if (yl < 0 && qv[j] > 0 && acc > t) yl = (int)(k * E + j);
                     }
                     if (yl < 0) yl = lpos;
                 }
@@ -318,11 +475,26 @@ __device__ __forceinline__ int rescan_segment(const void* rq, const void* rp, in
     return y >= 0 ? y : ylast;
 }
 
+// exponent l a - K as a df (a = ah + al), l finite
+__device__ __forceinline__ df exponent_df(float l, float ah, float al, float K) {
+    df e = two_prod(l, ah);
+    e = df_add_f(e, __fmul_rn(l, al));
+    return df_add_f(e, -K);
+}
+
+// power-of-two scale putting the largest weight just below 2^40
+__device__ __forceinline__ float fixed_scale(float wmax) {
+    int e;
+    frexpf(wmax, &e);   // wmax = m 2^e, m in [0.5, 1)
+    return pow2_int((float)(40 - e));
+}
+
 // ---------------------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------------------
 template <typename DQ, typename DP, int E>
 __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams p) {
+    extern __shared__ __align__(16) char ring_smem[];
     __shared__ Shared sh;
     cg::cluster_group cluster = cg::this_cluster();
     const int C = (int)cluster.num_blocks();
@@ -333,55 +505,101 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     const int64_t c0 = min(p.nchunk, (int64_t)(crank * kWarps + warp) * p.seg_chunks);
     const int64_t c1 = min(p.nchunk, c0 + p.seg_chunks);
     const int64_t V = p.V;
+    Feed<DQ, DP, E> feed;
+    feed.base = ring_smem + warp * Feed<DQ, DP, E>::RING;
+    feed.lane = lane;
 
-    // ---- stream header: offsets, temperature, tokens (identical in every CTA)
-    if (tid == 0) {
-        int st = SPEC_ST_OK;
-        const int base = p.cu[b];
-        const int n = p.cu[b + 1] - base;
-        if (n < 0 || n > p.kmax) st = SPEC_ST_BAD_OFFSETS;
-        const float T = p.temp[b];
-        if (st == SPEC_ST_OK && !(isfinite(T) && (T == 0.f || T >= FLT_MIN)))
-            st = SPEC_ST_BAD_TEMPERATURE;
-        const int nn = (st == SPEC_ST_BAD_OFFSETS) ? 0 : n;
-        if (st == SPEC_ST_OK) {
-            for (int i = 0; i < nn; ++i) {
-                const int xi = p.tokens[base + i];
-                sh.x[i] = xi;
-                if (xi < 0 || xi >= p.V) st = SPEC_ST_BAD_TOKEN;
-            }
-        }
-        sh.N = nn;
-        sh.status = st;
-        sh.greedy = (st == SPEC_ST_OK && T == 0.f);
-        sh.a = (st == SPEC_ST_OK && T > 0.f) ? (float)(kLog2e / (double)T) : 0.f;
-        sh.tau = 0;
-        sh.done = 0;
-    }
-    __syncthreads();
-    const int N = sh.N;
-    const float a = sh.a;
-    const bool greedy = sh.greedy;
-    const int64_t dbase = (sh.status == SPEC_ST_BAD_OFFSETS) ? 0 : p.cu[b];
+    // ---- stream header (identical in every CTA): offsets, temperature, tokens, and the draft
+    // and target logits at each draft token (loaded now, consumed after the sweep)
+    const int base = p.cu[b];
+    const int n_raw = p.cu[b + 1] - base;
+    const bool offsets_ok = n_raw >= 0 && n_raw <= p.kmax;
+    const int N = offsets_ok ? n_raw : 0;
+    const float T = p.temp[b];
+    const bool temp_ok = isfinite(T) && (T == 0.f || T >= FLT_MIN);
+    const bool greedy = (T == 0.f);
+    const int64_t dbase = offsets_ok ? base : 0;
     const int64_t tbase = dbase + b;
     auto qrow = [&](int i) { return row_ptr<DQ>(p.dq, dbase + i, V); };
     auto prow = [&](int i) { return row_ptr<DP>(p.dp, tbase + i, V); };
-    const int nrows = 2 * N + 1;  // part index: draft row i -> i, target row i -> N + i
+    bool bad_tok = false;
+    if (offsets_ok && temp_ok && tid < N) {
+        const int xi = p.tokens[base + tid];
+        sh.x[tid] = xi;
+        bad_tok = (xi < 0 || xi >= p.V);
+        if (!bad_tok && !greedy) {
+            sh.lq[tid] = load_elem<DQ>(qrow(tid), xi);
+            sh.lp[tid] = load_elem<DP>(prow(tid), xi);
+        }
+    }
+    bad_tok = __syncthreads_or(bad_tok);
+    if (tid == 0) {
+        int st = SPEC_ST_OK;
+        if (!offsets_ok) st = SPEC_ST_BAD_OFFSETS;
+        else if (!temp_ok) st = SPEC_ST_BAD_TEMPERATURE;
+        else if (bad_tok) st = SPEC_ST_BAD_TOKEN;
+        sh.N = N;
+        sh.status = st;
+        sh.greedy = (st == SPEC_ST_OK && greedy);
+        float ah = 0.f, al = 0.f;
+        if (st == SPEC_ST_OK && T > 0.f) {   // a = log2(e) / T as a df
+            const df l2e{1.4426950216293335f, 1.925963033500011e-08f};
+            const df q = df_div(l2e, df_make(T));
+            ah = q.hi;
+            al = q.lo;
+        }
+        sh.a_hi = ah;
+        sh.a_lo = al;
+        sh.tau = 0;
+        sh.sample_seg = -1;
+        sh.sample_bonus = 0;
+        sh.n_pass = 0;
+    }
+    __syncthreads();
+    const float ah = sh.a_hi, al = sh.a_lo;
+    const int nrows = 2 * N + 1;   // part index: draft row i -> i, target row i -> N + i
 
     if (sh.status == SPEC_ST_OK) {
-        // ---- stats sweep: bonus row first, then pairs 1..N-1, then pair 0
+        // ---- one sweep over every row of the stream
         if (!greedy) {
-            stats_single<DP, E, true>(prow(N), c0, c1, a, lane, &sh.part[2 * N][warp]);
-            for (int j = 1; j <= N; ++j) {
-                const int i = (j < N) ? j : 0;
-                stats_pair<DQ, DP, E>(qrow(i), prow(i), c0, c1, a, lane, &sh.part[i][warp],
-                                      &sh.part[N + i][warp]);
-            }
+            // items: 0 = bonus row N alone, 1..N-1 = pairs 1..N-1, N = pair 0
+            auto slot_of = [&](int it) { return it == 0 ? N : (it < N ? it : 0); };
+            LaneSum<E> aq, ap;
+            bool has_q = false;
+            sweep<DQ, DP, E>(
+                feed, N + 1, c0, c1, lane,
+                [&](int it, const void*& rq, const void*& rp) {
+                    const int i = slot_of(it);
+                    rq = (it == 0) ? nullptr : qrow(i);
+                    rp = prow(i);
+                },
+                [&](int it) { has_q = (it != 0); },
+                [&](int64_t, const float (&xq)[E], const float (&xp)[E]) {
+                    if (has_q) aq.add(xq, ah, al);
+                    ap.add(xp, ah, al);
+                },
+                [&](int it) {
+                    const int i = slot_of(it);
+                    if (it != 0) aq.publish(&sh.part[i][warp], lane);
+                    ap.publish(&sh.part[N + i][warp], lane);
+                    aq = LaneSum<E>();
+                    ap = LaneSum<E>();
+                });
         } else {
-            for (int i = 0; i <= N; ++i)
-                stats_single<DP, E, false>(prow(i), c0, c1, 0.f, lane, &sh.part[N + i][warp]);
+            LaneMax<E> am;
+            sweep<DQ, DP, E>(
+                feed, N + 1, c0, c1, lane,
+                [&](int it, const void*& rq, const void*& rp) {
+                    rq = nullptr;
+                    rp = prow(it);
+                },
+                [&](int) {},
+                [&](int64_t k, const float (&)[E], const float (&xp)[E]) { am.add(xp, k * E); },
+                [&](int it) {
+                    am.publish(&sh.part[N + it][warp], lane);
+                    am = LaneMax<E>();
+                });
         }
-        __syncthreads();
         cluster_sync_all();
 
         // ---- cluster reduction of the per-segment partials (same order in every CTA)
@@ -390,58 +608,74 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const int s = lane + 32 * k;
-                if (s < nseg) {
-                    const Part* src = cluster.map_shared_rank(&sh.part[r][s % kWarps], s / kWarps);
-                    e[k] = *src;
-                } else {
-                    e[k] = Part{-kInf, 0.f, INT_MAX};
-                }
+                if (s < nseg)
+                    e[k] = *cluster.map_shared_rank(&sh.part[r][s % kWarps], s / kWarps);
+                else
+                    e[k] = Part{greedy ? -kInf : kNoRef, 0.f, 0.f, INT_MAX};
             }
-            const float M = warp_max_nan(fmax_nan(e[0].m, e[1].m));
-            double z = 0.0;
-            double sc[2];
+            if (greedy) {
+                const float Kr = warp_max_nan(fmax_nan(e[0].K, e[1].K));
+                const int arg = warp_min_i(min(e[0].K == Kr ? e[0].idx : INT_MAX, e[1].K == Kr ? e[1].idx : INT_MAX));
+                if (lane == 0) {
+                    sh.rowK[r] = Kr;
+                    sh.rowArg[r] = arg;
+                    sh.rowZ[r] = df{0.f, 0.f};
+                }
+                continue;
+            }
+            const float Kr = warp_max(fmaxf(e[0].K, e[1].K));
+            df z{0.f, 0.f};
+            float segw[2];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-                sc[k] = (e[k].m == -kInf || greedy) ? 0.0 : (double)(e[k].s * ex2((e[k].m - M) * a));
-                z += sc[k];
+                const float sc = (e[k].K == Kr) ? 1.f : pow2_int(e[k].K - Kr);
+                const df v = df_scale(df{e[k].s_hi, e[k].s_lo}, sc);
+                segw[k] = df_to_f(v);
+                z = df_add(z, v);
             }
-            z = warp_sum_d(z);
-            const int arg = warp_min_i(min(e[0].m == M ? e[0].idx : INT_MAX,
-                                           e[1].m == M ? e[1].idx : INT_MAX));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const df other{__shfl_xor_sync(0xffffffffu, z.hi, o), __shfl_xor_sync(0xffffffffu, z.lo, o)};
+                z = df_add(z, other);
+            }
             if (lane == 0) {
-                sh.row_m[r] = M;
-                sh.row_z[r] = z;
-                sh.row_arg[r] = arg;
+                sh.rowK[r] = Kr;
+                sh.rowZ[r] = z;
+                sh.rowArg[r] = INT_MAX;
             }
-            if (r == 2 * N && !greedy) {
+            if (r == 2 * N) {
 #pragma unroll
                 for (int k = 0; k < 2; ++k)
-                    if (lane + 32 * k < nseg) sh.bonus_w[lane + 32 * k] = sc[k];
+                    if (lane + 32 * k < nseg) sh.bonus_w[lane + 32 * k] = segw[k];
             }
         }
         __syncthreads();
 
-        // ---- validity of the rows read, and q_i(x_i) > 0
+        // ---- validity of the rows read, q_i(x_i) > 0, per-slot ratios and uniforms
         bool bad_row = false, zero_q = false;
         for (int r = (greedy ? N : 0) + tid; r < nrows; r += kThreads) {
-            const float M = sh.row_m[r];
-            bad_row |= !isfinite(M) || !isfinite(sh.row_z[r]) || !(greedy || sh.row_z[r] > 0.0);
+            const float K = sh.rowK[r];
+            const df z = sh.rowZ[r];
+            bad_row |= greedy ? !isfinite(K) : !(isfinite(K) && K > kNoRef && isfinite(z.hi) && z.hi > 0.f);
         }
         if (!greedy && tid < N) {
-            const int xi = sh.x[tid];
-            const float lq = load_elem<DQ>(qrow(tid), xi);
-            const float lp = load_elem<DP>(prow(tid), xi);
+            const float lq = sh.lq[tid], lp = sh.lp[tid];
             zero_q = (lq == -kInf);
-            const double a64 = (double)a;
-            const double lzp = log2(sh.row_z[N + tid]);
-            const double lzq = log2(sh.row_z[tid]);
-            sh.log2px[tid] = ((double)lp - (double)sh.row_m[N + tid]) * a64 - lzp;
-            sh.log2qx[tid] = ((double)lq - (double)sh.row_m[tid]) * a64 - lzq;
+            const float Kq = sh.rowK[tid], Kp = sh.rowK[N + tid];
+            df rho{0.f, 0.f};
+            if (!zero_q && isfinite(lq) && isfinite(lp) && isfinite(Kq) && isfinite(Kp)) {
+                const df e = df_sub(exponent_df(lp, ah, al, Kp), exponent_df(lq, ah, al, Kq));
+                rho = df_div(df_mul(df_exp2(e), sh.rowZ[tid]), sh.rowZ[N + tid]);
+            }
+            sh.rho[tid] = rho;
         }
         if (!greedy && tid <= N) {
-            const double2 u = slot_uniforms(p.seed, p.step, (uint32_t)b, (uint32_t)tid);
-            sh.u_acc[tid] = u.x;
-            sh.u_smp[tid] = u.y;
+            const uint4 c = make_uint4((uint32_t)tid, (uint32_t)b, (uint32_t)p.step, (uint32_t)(p.step >> 32));
+            const uint4 wds = philox4x32_10(c, make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
+            sh.u_acc[tid] = uniform24_df(wds.x);
+            sh.u_smp[tid] = wds.y;
+            sh.h[tid] = df{__int_as_float(0x7fffffff), 0.f};
+            sh.r[tid] = df{__int_as_float(0x7fffffff), 0.f};
         }
         bad_row = __syncthreads_or(bad_row);
         zero_q = __syncthreads_or(zero_q);
@@ -449,147 +683,208 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
             if (bad_row) sh.status = SPEC_ST_BAD_ROW;
             else if (zero_q) sh.status = SPEC_ST_ZERO_DRAFT_PROB;
         }
-        if (!greedy && tid < N) sh.rho[tid] = exp2(sh.log2px[tid] - sh.log2qx[tid]);
         __syncthreads();
     }
 
+    const df one{1.f, 0.f};
+    int np = 0;
     // ---- decisions
     if (sh.status == SPEC_ST_OK && greedy) {
         if (tid == 0) {
             int tau = N;
             for (int i = 0; i < N; ++i)
-                if (sh.row_arg[N + i] != sh.x[i]) { tau = i; break; }
+                if (sh.rowArg[N + i] != sh.x[i]) {
+                    tau = i;
+                    break;
+                }
             sh.tau = tau;
         }
         __syncthreads();
     } else if (sh.status == SPEC_ST_OK) {
         const bool block = (p.rule == 1);
-        if (tid <= N) {
-            sh.h[tid] = nan("");
-            sh.r[tid] = nan("");
-        }
-        if (block) {
-            if (tid == 0) {
-                sh.log2w[0] = 0.0;
-                for (int i = 0; i < N; ++i)
-                    sh.log2w[i + 1] = fmin(0.0, sh.log2w[i] + (sh.log2px[i] - sh.log2qx[i]));
-            }
-            __syncthreads();
-            if (tid <= N) sh.w[tid] = exp2(sh.log2w[tid]);
-            __syncthreads();
-            if (tid == 0) {
-                // u_acc[i-1] is eta_i
-                if (N == 0) {
-                    sh.tau = 0; sh.done = 1;       // bonus only
+        if (tid == 0) {
+            int n = 0;
+            if (block) {
+                sh.w[0] = one;
+                for (int i = 0; i < N; ++i) sh.w[i + 1] = df_min(one, df_mul(sh.w[i], sh.rho[i]));
+                sh.tau = 0;
+                if (N > 0) sh.h[N] = sh.w[N];
+                if (N > 0 && df_le(sh.u_acc[N - 1], sh.h[N])) {
+                    sh.tau = N;   // eta_N <= w_N: accept everything, no residual needed
                 } else {
-                    sh.h[N] = sh.w[N];
-                    if (sh.u_acc[N - 1] <= sh.h[N]) { sh.tau = N; sh.done = 1; }
-                    else { sh.pass_slot = N; sh.done = 0; }
+                    for (int i = N - 1; i >= 1; --i)   // candidates: eta_i <= w_i (h_i <= w_i)
+                        if (df_le(sh.u_acc[i - 1], sh.w[i])) sh.pass_list[n++] = i;
+                    if (N > 0) sh.pass_list[n++] = 0;
+                }
+            } else {
+                int tau = N;
+                for (int i = 0; i < N; ++i)
+                    if (!df_le(sh.u_acc[i], df_min(one, sh.rho[i]))) {
+                        tau = i;
+                        break;
+                    }
+                sh.tau = tau;
+                if (tau < N) {
+                    sh.w[tau] = one;
+                    sh.pass_list[n++] = tau;
                 }
             }
-        } else if (tid == 0) {
-            int tau = N;
-            for (int i = 0; i < N; ++i)
-                if (!(sh.u_acc[i] <= fmin(1.0, sh.rho[i]))) { tau = i; break; }
-            sh.tau = tau;
-            sh.done = (tau == N);
-            sh.pass_slot = tau;
-            if (tau < N) { sh.w[tau] = 1.0; }
+            sh.n_pass = n;
+        }
+        __syncthreads();
+        np = sh.n_pass;
+        if (tid < np) {
+            const int i = sh.pass_list[tid];
+            sh.cval[i] = df_to_f(df_div(df_mul(sh.w[i], sh.rowZ[i]), sh.rowZ[N + i]));
         }
         __syncthreads();
 
-        // ---- residual sweeps (cluster-wide, lazily, at most N + 1)
-        int phase = 0;
-        while (true) {
-            if (tid == 0 && !sh.done && block) {
-                // next candidate below the last one tried
-                int i = sh.pass_slot - 1;
-                while (i >= 1 && sh.u_acc[i - 1] > sh.w[i]) --i;
-                sh.pass_slot = i;   // i == 0: tau = 0 and slot 0's residual is needed
-            }
-            __syncthreads();
-            if (sh.done) break;
-            const int i = sh.pass_slot;
-            const float mq = sh.row_m[i], mp = sh.row_m[N + i];
-            const float cc = (float)(sh.w[i] * sh.row_z[i] / sh.row_z[N + i]);
-            const float ws = residual_sum<DQ, DP, E>(qrow(i), prow(i), c0, c1, mq, mp, a, cc, lane);
-            if (lane == 0) sh.res_part[phase][warp] = ws;
-            __syncthreads();
+        // ---- one cluster-wide residual sweep over every slot that may be needed
+        if (np > 0) {
+            Kahan acc;
+            float Kq = 0.f, Kp = 0.f, cc = 0.f;
+            sweep<DQ, DP, E>(
+                feed, np, c0, c1, lane,
+                [&](int it, const void*& rq, const void*& rp) {
+                    const int i = sh.pass_list[it];
+                    rq = qrow(i);
+                    rp = prow(i);
+                },
+                [&](int it) {
+                    const int i = sh.pass_list[it];
+                    Kq = sh.rowK[i];
+                    Kp = sh.rowK[N + i];
+                    cc = sh.cval[i];
+                    acc = Kahan();
+                },
+                [&](int64_t, const float (&xq)[E], const float (&xp)[E]) {
+                    float w[E];
+                    resid_weights<E>(xq, xp, Kq, Kp, ah, al, cc, w);
+                    acc.add(chunk_sum<E>(w));
+                },
+                [&](int it) {
+                    df tot = acc.value();
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const df other{__shfl_xor_sync(0xffffffffu, tot.hi, o), __shfl_xor_sync(0xffffffffu, tot.lo, o)};
+                        tot = df_add(tot, other);
+                    }
+                    if (lane == 0) sh.res_part[it][warp] = df_to_f(tot);
+                });
             cluster_sync_all();
-            if (warp == 0) {
-                double tot = 0.0;
+            // per pass item: r_i = (sum over all segments) / Z_q
+            for (int it = warp; it < np; it += kWarps) {
+                df tot{0.f, 0.f};
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int s = lane + 32 * k;
-                    double v = 0.0;
-                    if (s < nseg)
-                        v = (double)*cluster.map_shared_rank(&sh.res_part[phase][s % kWarps], s / kWarps);
-                    if (s < kMaxSeg) sh.seg_w[s] = v;
-                    tot += v;
+                    const float v = (s < nseg) ? *cluster.map_shared_rank(&sh.res_part[it][s % kWarps], s / kWarps) : 0.f;
+                    tot = df_add_f(tot, v);
                 }
-                tot = warp_sum_d(tot);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const df other{__shfl_xor_sync(0xffffffffu, tot.hi, o), __shfl_xor_sync(0xffffffffu, tot.lo, o)};
+                    tot = df_add(tot, other);
+                }
                 if (lane == 0) {
-                    sh.resid_R = tot;
-                    const double ri = tot / sh.row_z[i];
+                    const int i = sh.pass_list[it];
+                    const df ri = df_div(tot, sh.rowZ[i]);
                     sh.r[i] = ri;
-                    if (!block || i == 0) {
-                        sh.tau = i;
-                        sh.done = 1;
-                    } else {
-                        const double den = ri + 1.0 - sh.w[i];
-                        const double hi = (den == 0.0) ? 1.0 : ri / den;
-                        sh.h[i] = hi;
-                        if (sh.u_acc[i - 1] <= hi) { sh.tau = i; sh.done = 1; }
+                    if (block && i >= 1) {
+                        const df den = df_add(ri, df_sub(one, sh.w[i]));
+                        sh.h[i] = df_is_zero(den) ? one : df_div(ri, den);
                     }
                 }
             }
             __syncthreads();
-            phase ^= 1;
-            if (sh.done) break;
+            if (tid == 0 && block) {
+                int tau = 0;
+                for (int it = 0; it < np; ++it) {   // candidates in descending order, then slot 0
+                    const int i = sh.pass_list[it];
+                    if (i >= 1 && df_le(sh.u_acc[i - 1], sh.h[i])) {
+                        tau = i;
+                        break;
+                    }
+                }
+                sh.tau = tau;
+            }
+            __syncthreads();
         }
 
-        // ---- the draw: coarse CDF over segments, then the owner warp rescans
-        if (tid == 0) {
+        // ---- the draw: 64-bit fixed-point CDF over the segments (warp 0)
+        if (warp == 0) {
             const int tau = sh.tau;
             const bool bonus = (tau == N);
-            const double* wseg = bonus ? sh.bonus_w : sh.seg_w;
-            double R = 0.0;
-            for (int s = 0; s < nseg; ++s) R += wseg[s];
-            sh.sample_bonus = bonus;
-            if (!(R > 0.0) || !isfinite(R)) {
-                sh.status = SPEC_ST_NUMERIC;
-                sh.sample_seg = -1;
+            int item = 0;
+            for (int it = 0; it < np; ++it)
+                if (sh.pass_list[it] == tau) item = it;
+            float w0 = 0.f, w1 = 0.f;
+            if (bonus) {
+                if (lane < nseg) w0 = sh.bonus_w[lane];
+                if (lane + 32 < nseg) w1 = sh.bonus_w[lane + 32];
             } else {
-                const double t = sh.u_smp[tau] * R;
-                double cum = 0.0;
-                int seg = -1, lastpos = -1;
-                double tr = 0.0;
-                for (int s = 0; s < nseg; ++s) {
-                    if (wseg[s] > 0.0) {
-                        lastpos = s;
-                        if (seg < 0 && cum + wseg[s] >= t) { seg = s; tr = t - cum; }
-                    }
-                    cum += wseg[s];
+                if (lane < nseg) w0 = *cluster.map_shared_rank(&sh.res_part[item][lane % kWarps], lane / kWarps);
+                if (lane + 32 < nseg)
+                    w1 = *cluster.map_shared_rank(&sh.res_part[item][(lane + 32) % kWarps], (lane + 32) / kWarps);
+            }
+            const float wmax = warp_max(fmaxf(w0, w1));
+            const bool ok = isfinite(wmax) && wmax > 0.f;
+            const float scale = ok ? fixed_scale(wmax) : 0.f;
+            const unsigned long long q0 = ok ? __float2ull_rn(w0 * scale) : 0ull;
+            const unsigned long long q1 = ok ? __float2ull_rn(w1 * scale) : 0ull;
+            unsigned long long p0 = q0, p1 = q1;   // inclusive prefix sums
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long n0 = __shfl_up_sync(0xffffffffu, p0, o);
+                const unsigned long long n1 = __shfl_up_sync(0xffffffffu, p1, o);
+                if (lane >= o) {
+                    p0 += n0;
+                    p1 += n1;
                 }
-                if (seg < 0) { seg = lastpos; tr = wseg[lastpos]; }
-                sh.sample_seg = seg;
-                sh.sample_t = tr;
+            }
+            p1 += __shfl_sync(0xffffffffu, p0, 31);
+            const unsigned long long R = __shfl_sync(0xffffffffu, p1, 31);
+            // t = floor(U R), U = (2k + 1) 2^-25 with k the word's top 24 bits
+            const unsigned long long odd = 2ull * (sh.u_smp[tau] >> 8) + 1ull;
+            const unsigned long long t = (__umul64hi(odd, R) << 39) | ((odd * R) >> 25);
+            const unsigned h0 = __ballot_sync(0xffffffffu, q0 > 0 && p0 > t);
+            const unsigned h1 = __ballot_sync(0xffffffffu, q1 > 0 && p1 > t);
+            const int seg = h0 ? __ffs(h0) - 1 : (h1 ? 32 + __ffs(h1) - 1 : -1);
+            const int src = seg < 0 ? 0 : seg % 32;
+            const unsigned long long i0 = __shfl_sync(0xffffffffu, p0, src);
+            const unsigned long long i1 = __shfl_sync(0xffffffffu, p1, src);
+            const unsigned long long qs0 = __shfl_sync(0xffffffffu, q0, src);
+            const unsigned long long qs1 = __shfl_sync(0xffffffffu, q1, src);
+            if (lane == 0) {
+                if (ok && R > 0 && seg >= 0) {
+                    const unsigned long long excl = (seg < 32) ? i0 - qs0 : i1 - qs1;
+                    sh.sample_t = t - excl;
+                    sh.sample_scale = scale;
+                    sh.sample_seg = seg;
+                    sh.sample_bonus = bonus;
+                } else {
+                    sh.status = SPEC_ST_NUMERIC;
+                    sh.sample_seg = -1;
+                }
             }
         }
         __syncthreads();
-        if (sh.status == SPEC_ST_OK && sh.sample_seg == crank * kWarps + warp) {
-            const int tau = sh.tau;
-            int y;
-            if (sh.sample_bonus) {
-                y = rescan_segment<DQ, DP, E, true>(nullptr, prow(N), c0, c1, 0.f, sh.row_m[2 * N],
-                                                    a, 0.f, sh.sample_t, lane);
-            } else {
-                const float cc = (float)(sh.w[tau] * sh.row_z[tau] / sh.row_z[N + tau]);
-                y = rescan_segment<DQ, DP, E, false>(qrow(tau), prow(tau), c0, c1, sh.row_m[tau],
-                                                     sh.row_m[N + tau], a, cc, sh.sample_t, lane);
-            }
-            if (lane == 0) p.out_tok[(int64_t)b * (p.kmax + 1) + tau] = y;
+    }
+
+    // every distributed-shared-memory read of this CTA is done: arrive now, wait at the end
+    cluster_arrive();
+
+    if (sh.status == SPEC_ST_OK && !greedy && sh.sample_seg == crank * kWarps + warp) {
+        const int tau = sh.tau;
+        int y;
+        if (sh.sample_bonus) {
+            y = rescan_segment<DQ, DP, E, true>(nullptr, prow(N), c0, c1, 0.f, sh.rowK[2 * N], ah, al, 0.f,
+                                                sh.sample_scale, sh.sample_t, lane);
+        } else {
+            y = rescan_segment<DQ, DP, E, false>(qrow(tau), prow(tau), c0, c1, sh.rowK[tau], sh.rowK[N + tau], ah,
+                                                 al, sh.cval[tau], sh.sample_scale, sh.sample_t, lane);
         }
+        if (lane == 0) p.out_tok[(int64_t)b * (p.kmax + 1) + tau] = y;
     }
 
     // ---- outputs (CTA rank 0)
@@ -601,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
             if (st != SPEC_ST_OK) p.out_tok[ob + j] = -1;
             else if (j < tau) p.out_tok[ob + j] = sh.x[j];
             else if (j > tau) p.out_tok[ob + j] = -1;
-            else if (greedy) p.out_tok[ob + j] = sh.row_arg[N + tau];
+            else if (sh.greedy) p.out_tok[ob + j] = sh.rowArg[N + tau];
         }
         if (tid == 0) {
             p.status[b] = st;
@@ -610,26 +905,32 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
         }
         if (p.diag != nullptr && st != SPEC_ST_BAD_OFFSETS) {
             const float qnan = __int_as_float(0x7fffffff);
-            const bool have = (!greedy) && (st == SPEC_ST_OK || st == SPEC_ST_NUMERIC);
+            const float ln2 = 0.6931471805599453f;
+            const bool have = (!sh.greedy) && (st == SPEC_ST_OK || st == SPEC_ST_NUMERIC);
             for (int i = tid; i <= N; i += kThreads) {
                 float* d = p.diag + (tbase + i) * SPEC_DIAG_COLS;
                 float v[SPEC_DIAG_COLS];
 #pragma unroll
                 for (int c = 0; c < SPEC_DIAG_COLS; ++c) v[c] = qnan;
                 if (have) {
-                    const double a64 = (double)a;
-                    v[SPEC_DIAG_LOGZP] = (float)(kLn2 * ((double)sh.row_m[N + i] * a64 + log2(sh.row_z[N + i])));
+                    // natural log of sum exp(l / T) = ln 2 (K + log2 Z)
+                    const df zp = sh.rowZ[N + i];
+                    v[SPEC_DIAG_LOGZP] = ln2 * (sh.rowK[N + i] + log2f(zp.hi)) + zp.lo / zp.hi;
                     if (i < N) {
-                        v[SPEC_DIAG_PX] = (float)exp2(sh.log2px[i]);
-                        v[SPEC_DIAG_QX] = (float)exp2(sh.log2qx[i]);
-                        v[SPEC_DIAG_RHO] = (float)sh.rho[i];
-                        v[SPEC_DIAG_LOGZQ] = (float)(kLn2 * ((double)sh.row_m[i] * a64 + log2(sh.row_z[i])));
+                        const df zq = sh.rowZ[i];
+                        const float lq = sh.lq[i], lp = sh.lp[i];
+                        v[SPEC_DIAG_PX] =
+                            isfinite(lp) ? df_to_f(df_div(df_exp2(exponent_df(lp, ah, al, sh.rowK[N + i])), zp)) : 0.f;
+                        v[SPEC_DIAG_QX] =
+                            isfinite(lq) ? df_to_f(df_div(df_exp2(exponent_df(lq, ah, al, sh.rowK[i])), zq)) : 0.f;
+                        v[SPEC_DIAG_RHO] = df_to_f(sh.rho[i]);
+                        v[SPEC_DIAG_LOGZQ] = ln2 * (sh.rowK[i] + log2f(zq.hi)) + zq.lo / zq.hi;
                     }
                     if (p.rule == 1) {
-                        v[SPEC_DIAG_W] = (float)sh.w[i];
-                        if (i >= 1) v[SPEC_DIAG_H] = (float)sh.h[i];
+                        v[SPEC_DIAG_W] = df_to_f(sh.w[i]);
+                        if (i >= 1) v[SPEC_DIAG_H] = df_to_f(sh.h[i]);
                     }
-                    v[SPEC_DIAG_R] = (float)sh.r[i];
+                    v[SPEC_DIAG_R] = df_to_f(sh.r[i]);
                 }
 #pragma unroll
                 for (int c = 0; c < SPEC_DIAG_COLS; ++c) d[c] = v[c];
@@ -637,10 +938,10 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
         }
     }
     // no CTA may leave while another can still read its shared memory
-    cluster_sync_all();
+    cluster_wait();
 }
 
-// Uniforms exposed for checking: out[(s * n_slots + i) * 2 + {0, 1}]
+// Uniforms exposed for checking: out[(s * n_slots + i) * 2 + {0, 1}] (exact in double)
 __global__ void philox_uniforms_kernel(uint64_t seed, uint64_t step, int n_streams, int n_slots,
                                        double* out) {
     const int64_t total = (int64_t)n_streams * n_slots;
@@ -656,40 +957,48 @@ __global__ void philox_uniforms_kernel(uint64_t seed, uint64_t step, int n_strea
 // Host side
 // ---------------------------------------------------------------------------------------
 template <typename DQ, typename DP, int E>
-static cudaError_t launch_verify(const VerifyParams& p, int C, cudaStream_t s) {
+static size_t ring_bytes() {
+    return (size_t)kWarps * Feed<DQ, DP, E>::RING;
+}
+
+template <typename DQ, typename DP, int E>
+static cudaLaunchConfig_t make_config(int grid, int C, cudaStream_t s, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.B * C));
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = ring_bytes<DQ, DP, E>();
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, verify_kernel<DQ, DP, E>, p);
+    return cfg;
 }
 
-// How many clusters of C CTAs fit on the device at once (queried once per kernel and C).
+template <typename DQ, typename DP, int E>
+static cudaError_t prepare_kernel() {
+    static int done[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    if (done[dev]) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(verify_kernel<DQ, DP, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)ring_bytes<DQ, DP, E>());
+    if (e == cudaSuccess) done[dev] = 1;
+    return e;
+}
+
+// How many clusters of C CTAs fit on the device at once (queried once per kernel, C, device).
 template <typename DQ, typename DP, int E>
 static int resident_clusters(int C) {
-    static int cache[kMaxCluster + 1][64] = {};   // [C][device]
+    static int cache[kMaxCluster + 1][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
     int& slot = cache[C][dev];
     if (slot == 0) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)C);
-        cfg.blockDim = dim3(kThreads);
         cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)C;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cudaLaunchConfig_t cfg = make_config<DQ, DP, E>(C, C, nullptr, attr);
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, verify_kernel<DQ, DP, E>, &cfg) != cudaSuccess || n < 1) {
             cudaGetLastError();
@@ -722,39 +1031,46 @@ static int pick_cluster(int B, int64_t nchunk) {
 }
 
 template <typename DQ, typename DP, int E>
-static cudaError_t run_verify(VerifyParams& p, cudaStream_t s) {
+static cudaError_t run_verify(VerifyParams& p, cudaStream_t s, int* info) {
+    cudaError_t e = prepare_kernel<DQ, DP, E>();
+    if (e != cudaSuccess) return e;
     const int C = pick_cluster<DQ, DP, E>(p.B, p.nchunk);
     p.seg_chunks = (p.nchunk + (int64_t)C * kWarps - 1) / ((int64_t)C * kWarps);
-    return launch_verify<DQ, DP, E>(p, C, s);
+    if (info) {
+        info[0] = C;
+        info[1] = resident_clusters<DQ, DP, E>(C);
+        return cudaSuccess;
+    }
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = make_config<DQ, DP, E>(p.B * C, C, s, attr);
+    return cudaLaunchKernelEx(&cfg, verify_kernel<DQ, DP, E>, p);
 }
 
 template <int E>
-static cudaError_t dispatch_dtypes(VerifyParams& p, int dq, int dp, cudaStream_t s) {
-    if (dq == SPEC_DTYPE_BF16 && dp == SPEC_DTYPE_BF16)
-        return run_verify<__nv_bfloat16, __nv_bfloat16, E>(p, s);
-    if (dq == SPEC_DTYPE_F32 && dp == SPEC_DTYPE_F32) return run_verify<float, float, E>(p, s);
-    if (dq == SPEC_DTYPE_F32 && dp == SPEC_DTYPE_BF16)
-        return run_verify<float, __nv_bfloat16, E>(p, s);
-    return run_verify<__nv_bfloat16, float, E>(p, s);
+static cudaError_t dispatch_dtypes(VerifyParams& p, int dq, int dp, cudaStream_t s, int* info) {
+    if (dq == SPEC_DTYPE_BF16 && dp == SPEC_DTYPE_BF16) return run_verify<__nv_bfloat16, __nv_bfloat16, E>(p, s, info);
+    if (dq == SPEC_DTYPE_F32 && dp == SPEC_DTYPE_F32) return run_verify<float, float, E>(p, s, info);
+    if (dq == SPEC_DTYPE_F32 && dp == SPEC_DTYPE_BF16) return run_verify<float, __nv_bfloat16, E>(p, s, info);
+    return run_verify<__nv_bfloat16, float, E>(p, s, info);
 }
 
-static int verify_entry(const spec_verify_args* a, void* stream, int rule, const char* name) {
+static int verify_entry(const spec_verify_args* a, void* stream, int rule, const char* name, int* info) {
     if (a == nullptr) return set_error(SPEC_ERR_ARG, "%s: args is NULL", name);
     if (a->B < 0) return set_error(SPEC_ERR_SHAPE, "%s: B = %d < 0", name, a->B);
     if (a->V < 1 || a->V > SPEC_MAX_V)
         return set_error(SPEC_ERR_SHAPE, "%s: V = %d outside [1, %d]", name, a->V, SPEC_MAX_V);
     if (a->kmax < 0 || a->kmax > SPEC_MAX_KMAX)
-        return set_error(SPEC_ERR_SHAPE, "%s: kmax = %d outside [0, %d]", name, a->kmax,
-                         SPEC_MAX_KMAX);
+        return set_error(SPEC_ERR_SHAPE, "%s: kmax = %d outside [0, %d]", name, a->kmax, SPEC_MAX_KMAX);
     if (!valid_dtype(a->draft_dtype) || !valid_dtype(a->target_dtype))
-        return set_error(SPEC_ERR_DTYPE, "%s: dtype must be SPEC_DTYPE_F32 or SPEC_DTYPE_BF16",
-                         name);
-    if (a->B == 0) return clear_error();
-    if (!a->cu_drafts || !a->target_logits || !a->temperature || !a->accepted_len ||
-        !a->out_tokens || !a->n_emitted || !a->status)
-        return set_error(SPEC_ERR_ARG, "%s: a required pointer is NULL", name);
-    if ((a->kmax > 0) && (!a->draft_logits || !a->draft_tokens))
-        return set_error(SPEC_ERR_ARG, "%s: draft_logits / draft_tokens is NULL", name);
+        return set_error(SPEC_ERR_DTYPE, "%s: dtype must be SPEC_DTYPE_F32 or SPEC_DTYPE_BF16", name);
+    if (info == nullptr) {
+        if (a->B == 0) return clear_error();
+        if (!a->cu_drafts || !a->target_logits || !a->temperature || !a->accepted_len || !a->out_tokens ||
+            !a->n_emitted || !a->status)
+            return set_error(SPEC_ERR_ARG, "%s: a required pointer is NULL", name);
+        if ((a->kmax > 0) && (!a->draft_logits || !a->draft_tokens))
+            return set_error(SPEC_ERR_ARG, "%s: draft_logits / draft_tokens is NULL", name);
+    }
     VerifyParams p;
     p.B = a->B;
     p.V = a->V;
@@ -776,33 +1092,46 @@ static int verify_entry(const spec_verify_args* a, void* stream, int rule, const
                          ((uintptr_t)a->draft_logits % 16 == 0);
     p.nchunk = aligned ? a->V / 8 : a->V;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = aligned ? dispatch_dtypes<8>(p, a->draft_dtype, a->target_dtype, s)
-                                  : dispatch_dtypes<1>(p, a->draft_dtype, a->target_dtype, s);
+    const cudaError_t e = aligned ? dispatch_dtypes<8>(p, a->draft_dtype, a->target_dtype, s, info)
+                                  : dispatch_dtypes<1>(p, a->draft_dtype, a->target_dtype, s, info);
     if (e != cudaSuccess) return set_cuda_error(e, name);
+    if (info) info[2] = aligned ? 8 : 1;
     return clear_error();
 }
 
 }  // namespace sv
 
 extern "C" int spec_verify_tokenwise(const spec_verify_args* args, void* stream) {
-    return sv::verify_entry(args, stream, 0, "spec_verify_tokenwise");
+    return sv::verify_entry(args, stream, 0, "spec_verify_tokenwise", nullptr);
 }
 
 extern "C" int spec_verify_block(const spec_verify_args* args, void* stream) {
-    return sv::verify_entry(args, stream, 1, "spec_verify_block");
+    return sv::verify_entry(args, stream, 1, "spec_verify_block", nullptr);
 }
 
-extern "C" int spec_philox_uniforms(uint64_t seed, uint64_t step, int32_t n_streams,
-                                    int32_t n_slots, double* out, void* stream) {
-    if (n_streams < 0 || n_slots < 0)
-        return sv::set_error(SPEC_ERR_SHAPE, "spec_philox_uniforms: negative count");
+extern "C" int spec_verify_launch_info(const spec_verify_args* args, int32_t* cluster_size,
+                                       int32_t* resident_clusters, int32_t* elems_per_load) {
+    if (!cluster_size || !resident_clusters || !elems_per_load)
+        return sv::set_error(SPEC_ERR_ARG, "spec_verify_launch_info: an output pointer is NULL");
+    int info[3] = {0, 0, 0};
+    const int rc = sv::verify_entry(args, nullptr, 1, "spec_verify_launch_info", info);
+    if (rc != SPEC_OK) return rc;
+    *cluster_size = info[0];
+    *resident_clusters = info[1];
+    *elems_per_load = info[2];
+    return SPEC_OK;
+}
+
+extern "C" int spec_philox_uniforms(uint64_t seed, uint64_t step, int32_t n_streams, int32_t n_slots,
+                                    double* out, void* stream) {
+    if (n_streams < 0 || n_slots < 0) return sv::set_error(SPEC_ERR_SHAPE, "spec_philox_uniforms: negative count");
     const int64_t total = (int64_t)n_streams * n_slots;
     if (total == 0) return sv::clear_error();
     if (out == nullptr) return sv::set_error(SPEC_ERR_ARG, "spec_philox_uniforms: out is NULL");
     const int64_t blocks64 = (total + 255) / 256;
     const int blocks = (int)(blocks64 < 4096 ? blocks64 : 4096);
-    sv::philox_uniforms_kernel<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        seed, step, n_streams, n_slots, out);
+    sv::philox_uniforms_kernel<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(seed, step, n_streams,
+                                                                                        n_slots, out);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return sv::set_cuda_error(e, "spec_philox_uniforms");
     return sv::clear_error();
