@@ -39,6 +39,8 @@ zero-weight token since U > 0).
 Which rows a rule reads (this decides which invalid rows raise a status):
   T > 0: all 2N+1 rows of the stream (draft rows 0..N-1, target rows 0..N);
   T = 0: the N+1 target rows only.
+Offsets: cu[0] = 0 and every draft count N_b = cu[b+1] - cu[b] in [0, kmax]; from the first
+stream that breaks this on, every stream is BAD_OFFSETS (its rows have no defined position).
 Status precedence per stream: BAD_OFFSETS, BAD_TEMPERATURE, BAD_TOKEN (any of the N draft
 tokens outside [0, V)), BAD_ROW (a read row with NaN / +inf / no finite entry),
 ZERO_DRAFT_PROB (T > 0 and q_i(x_i) = 0 at some slot), NUMERIC (zero residual mass where a
@@ -303,10 +305,19 @@ def verify_batch(rule, cu_drafts, draft_logits, target_logits, draft_tokens, tem
         "tie": np.zeros(B, bool),
         "tie_kind": [None] * B,
     }
+    # Streams are packed from row 0 in order.  The first stream whose draft count lies
+    # outside [0, kmax] (or cu[0] != 0) leaves the row positions of every later stream
+    # undefined, so from there on every stream is BAD_OFFSETS.
+    first_bad = B
+    for b in range(B):
+        n = cu[b + 1] - cu[b]
+        if n < 0 or n > kmax or (b == 0 and cu[0] != 0):
+            first_bad = b
+            break
     todo = range(B) if streams is None else streams
     for b in todo:
         n = cu[b + 1] - cu[b]
-        if n < 0 or n > kmax:
+        if b >= first_bad:
             out["status"][b] = STATUS_BAD_OFFSETS
             continue
         q_rows = [draft_logits[cu[b] + i] for i in range(n)]

@@ -127,6 +127,14 @@ def test_batch_layout_and_offsets():
                               inp["target_logits"], inp["draft_tokens"],
                               inp["temperature"][:2], kmax=2, seed=0, step=0)
     assert list(bad["status"]) == [verify.STATUS_BAD_OFFSETS, verify.STATUS_BAD_OFFSETS]
+    # a valid-looking stream after a broken one, and a batch that does not start at row 0
+    B5 = verify.STATUS_BAD_OFFSETS
+    for cu_bad, want in (([0, 2, 1, 6], [0, B5, B5]), ([0, 1, 5, 6], [0, B5, B5]),
+                         ([0, 5, 1, 2], [B5, B5, B5]), ([1, 2, 3, 4], [B5, B5, B5])):
+        r = verify.verify_batch(0, np.array(cu_bad), np.zeros((8, 4)), np.zeros((12, 4)),
+                                np.zeros(8, np.int32), np.ones(3, np.float32), kmax=2, seed=0,
+                                step=0)
+        assert list(r["status"]) == want, cu_bad
 
 
 def test_tokenwise_acceptance_rate_is_one_minus_tv():
