@@ -57,6 +57,7 @@ extern "C" {
 #define SPEC_ERR_SHAPE (-3)    /* size out of the supported range */
 #define SPEC_ERR_CUDA (-4)     /* a CUDA runtime call or launch failed */
 #define SPEC_ERR_DEVICE (-5)   /* the current device cannot run these kernels */
+#define SPEC_ERR_WORKSPACE (-6) /* workspace missing, too small or misaligned */
 
 /* per-stream status codes written by the verify calls (device data errors) */
 #define SPEC_ST_OK 0
@@ -64,7 +65,8 @@ extern "C" {
 #define SPEC_ST_BAD_TOKEN 2       /* a draft token of the stream lies outside [0, V) */
 #define SPEC_ST_BAD_ROW 3         /* a read logit row holds NaN or +inf, or has no finite entry */
 #define SPEC_ST_ZERO_DRAFT_PROB 4 /* T > 0 and q_i(x_i) = 0 (the draft logit at x_i is -inf) */
-#define SPEC_ST_BAD_OFFSETS 5     /* cu_drafts[b+1] - cu_drafts[b] is negative or above kmax */
+#define SPEC_ST_BAD_OFFSETS 5     /* cu_drafts[0] != 0, or the count of stream b or of an
+                                     earlier stream is negative or above kmax */
 #define SPEC_ST_TIMEOUT 6         /* reserved: a bounded device wait gave up */
 #define SPEC_ST_NUMERIC 7         /* the distribution to draw from has zero or non-finite mass */
 
@@ -105,7 +107,9 @@ int dspark_markov_bias(const void* draft_logits, int32_t draft_dtype, int32_t ro
 
 /*
  * Arguments shared by both verify calls.  B streams; stream b has
- * N_b = cu_drafts[b+1] - cu_drafts[b] drafts (0 <= N_b <= kmax).
+ * N_b = cu_drafts[b+1] - cu_drafts[b] drafts (0 <= N_b <= kmax), packed from row 0
+ * (cu_drafts[0] = 0).  From the first stream that breaks this on, every stream reports
+ * SPEC_ST_BAD_OFFSETS, since its rows no longer have a defined position.
  *   draft row of (b, i)  = cu_drafts[b] + i          (i < N_b)
  *   target row of (b, i) = cu_drafts[b] + b + i      (i <= N_b; i = N_b is the bonus slot)
  * Inputs (device): cu_drafts [B+1] int32; draft_logits [cu[B], V]; target_logits
@@ -115,6 +119,8 @@ int dspark_markov_bias(const void* draft_logits, int32_t draft_dtype, int32_t ro
  * n_emitted [B] int32 = tau + 1 (0 when status != 0); status [B] int32 (SPEC_ST_*).
  * diag is optional (NULL = not written): float [cu[B] + B, SPEC_DIAG_COLS], NaN where a
  * value was not computed.
+ * workspace: device scratch of at least spec_verify_workspace_bytes(B, kmax) bytes; calls that
+ * share a workspace must be ordered (same stream).
  * Rows read: T > 0 reads all 2 N_b + 1 rows of the stream; T = 0 reads the N_b + 1 target
  * rows only.  Status precedence: BAD_OFFSETS, BAD_TEMPERATURE, BAD_TOKEN, BAD_ROW,
  * ZERO_DRAFT_PROB, NUMERIC.
@@ -139,7 +145,17 @@ typedef struct {
     int32_t* n_emitted;
     int32_t* status;
     float* diag;
+    void* workspace;
+    size_t workspace_bytes;
 } spec_verify_args;
+
+/*
+ * spec_verify_workspace_bytes - device workspace a verify call over B streams with up to
+ * kmax drafts each needs (16-byte aligned, caller-allocated, contents need no initialisation;
+ * 0 for invalid arguments).  The workspace holds the per-segment row statistics that the
+ * stats pass hands to the per-stream pass; it may be reused by later calls on the same stream.
+ */
+size_t spec_verify_workspace_bytes(int32_t B, int32_t kmax);
 
 /*
  * spec_verify_tokenwise - token-by-token speculative sampling.
@@ -149,7 +165,8 @@ typedef struct {
  * from p_N.  p_i = softmax(target_i / T), q_i = softmax(draft_i / T).  Draws are inverse
  * CDF: the smallest v with C(v) >= U * R (ascending vocabulary order).
  * Errors: SPEC_ERR_ARG, SPEC_ERR_DTYPE, SPEC_ERR_SHAPE (B < 0, V < 1, V > SPEC_MAX_V,
- * kmax < 0 or kmax > SPEC_MAX_KMAX), SPEC_ERR_CUDA.  B == 0 launches nothing.
+ * kmax < 0 or kmax > SPEC_MAX_KMAX), SPEC_ERR_WORKSPACE, SPEC_ERR_CUDA.  B == 0 launches
+ * nothing.
  */
 int spec_verify_tokenwise(const spec_verify_args* args, void* stream);
 

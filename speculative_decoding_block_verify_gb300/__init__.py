@@ -22,7 +22,8 @@ import os
 
 __all__ = [
     "dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block", "adaptive_pick_k",
-    "spec_philox_uniforms", "spec_verify_launch_info", "lib", "lib_path", "SpecError",
+    "spec_philox_uniforms", "spec_verify_launch_info",
+    "spec_verify_workspace_bytes", "lib", "lib_path", "SpecError",
     "DTYPE_F32", "DTYPE_BF16", "STATUS_NAMES", "DIAG_COLS",
 ]
 
@@ -33,6 +34,7 @@ STATUS_NAMES = {0: "OK", 1: "BAD_TEMPERATURE", 2: "BAD_TOKEN", 3: "BAD_ROW",
                 4: "ZERO_DRAFT_PROB", 5: "BAD_OFFSETS", 6: "TIMEOUT", 7: "NUMERIC"}
 EXPORTED = ["dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block",
             "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info",
+            "spec_verify_workspace_bytes",
             "spec_last_error", "spec_version"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -59,6 +61,7 @@ class VerifyArgs(ctypes.Structure):
         ("accepted_len", ctypes.c_void_p), ("out_tokens", ctypes.c_void_p),
         ("n_emitted", ctypes.c_void_p), ("status", ctypes.c_void_p),
         ("diag", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -85,6 +88,8 @@ def lib():
     L.spec_philox_uniforms.argtypes = [u64, u64, i32, i32, vp, vp]
     L.spec_verify_launch_info.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.POINTER(i32),
                                           ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    L.spec_verify_workspace_bytes.argtypes = [i32, i32]
+    L.spec_verify_workspace_bytes.restype = ctypes.c_size_t
     L.spec_last_error.restype = ctypes.c_char_p
     L.spec_version.restype = ctypes.c_int32
     for name in ("dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block",
@@ -185,6 +190,10 @@ def _verify(fn, cu_drafts, draft_logits, target_logits, draft_tokens, temperatur
         if diag:
             out["diag"] = torch.empty((target_logits.shape[0], DIAG_COLS), dtype=torch.float32,
                                       device=dev)
+    need = spec_verify_workspace_bytes(B, kmax)
+    ws = out.get("workspace")
+    if ws is None or ws.numel() < need:
+        ws = out["workspace"] = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     a = VerifyArgs()
     a.B, a.V, a.kmax = B, V, kmax
     a.cu_drafts = cu_drafts.data_ptr()
@@ -201,6 +210,8 @@ def _verify(fn, cu_drafts, draft_logits, target_logits, draft_tokens, temperatur
     a.n_emitted = out["n_emitted"].data_ptr()
     a.status = out["status"].data_ptr()
     a.diag = out["diag"].data_ptr() if out.get("diag") is not None else None
+    a.workspace = ws.data_ptr()
+    a.workspace_bytes = ws.numel()
     _check(fn(ctypes.byref(a), _stream(stream)))
     return out
 
@@ -242,6 +253,11 @@ def adaptive_pick_k(hidden, w, bias, verify_ms, mode=0, out=None, stream=None):
                                  _ptr(out["c"]), _ptr(out["a"]), _ptr(out["k"]), _ptr(out["cu"]),
                                  _stream(stream)))
     return out
+
+
+def spec_verify_workspace_bytes(B, kmax):
+    """Device workspace bytes a verify call over B streams with up to kmax drafts needs."""
+    return int(lib().spec_verify_workspace_bytes(int(B), int(kmax)))
 
 
 def spec_verify_launch_info(B, V, kmax, draft_dtype=DTYPE_BF16, target_dtype=DTYPE_BF16,

@@ -46,9 +46,11 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 8;
 constexpr int kMaxRows = 2 * SPEC_MAX_KMAX + 1;
-constexpr int kMaxSeg = kMaxCluster * kWarps;
-constexpr int kRingBytesPerCta = 48 * 1024;
+constexpr int kRingBytesPerCta = 56 * 1024;
 constexpr float kNoRef = -1e30f;     // reference of a lane that has seen no finite logit
+constexpr int kPiecesMax = 64;       // stats partials per row
+
+struct Part;
 
 struct VerifyParams {
     int32_t B, V, kmax, rule;
@@ -64,7 +66,9 @@ struct VerifyParams {
     int32_t* status;
     float* diag;
     int64_t nchunk;      // chunks of 8 (or 1) elements per row
-    int64_t seg_chunks;  // chunks per warp segment
+    int64_t seg_chunks;  // chunks per warp segment of the cluster kernel's residual sweep
+    struct Part* part;   // workspace: per-row partials of the stats kernel, [rows][kPiecesMax]
+    int64_t stats_warps; // warps of the stats kernel's grid
 };
 
 // Per-warp partial of one row.  T > 0: K = integer reference, (s_hi, s_lo) = sum 2^(l a - K).
@@ -75,13 +79,17 @@ struct Part {
     int idx;
 };
 
+// bytes of workspace a verify call needs: kPiecesMax partials per row; a stream has at most
+// 2 kmax + 1 rows
+static size_t workspace_bytes(int32_t B, int32_t kmax) {
+    return (size_t)B * (size_t)(2 * kmax + 1) * kPiecesMax * sizeof(Part);
+}
+
 struct Shared {
-    Part part[kMaxRows][kWarps];
     float res_part[SPEC_MAX_KMAX + 1][kWarps];
     float rowK[kMaxRows];
     df rowZ[kMaxRows];
     int rowArg[kMaxRows];
-    float bonus_w[kMaxSeg];
     df rho[SPEC_MAX_KMAX];
     df w[SPEC_MAX_KMAX + 1];
     df h[SPEC_MAX_KMAX + 1];
@@ -93,6 +101,7 @@ struct Shared {
     int x[SPEC_MAX_KMAX];
     int pass_list[SPEC_MAX_KMAX + 1];
     int n_pass;
+    int to_flag[kWarps];            // a bounded wait of this warp gave up
     int N, status, greedy, tau, sample_seg, sample_bonus;
     unsigned long long sample_t;   // in-segment target (fixed point)
     float sample_scale;            // fixed-point scale of the draw's weights
@@ -111,24 +120,14 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // ---------------------------------------------------------------------------------------
-// cp.async helpers
-// ---------------------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// ---------------------------------------------------------------------------------------
 // Chunk feeds.  A stage is U chunks per lane of up to two rows (q and p): lane L of a warp
-// takes chunks k0 + u*32 + L, u < U.  The vector path (E = 8, 16-byte aligned rows) stages
-// through a per-warp cp.async ring of D stages; the plain path (E = 1) loads directly.
-// Each lane reads back only the bytes it copied, so the ring needs no barrier.
+// takes chunks rel + u*32 + L, u < U.  The vector path (E = 8, 16-byte aligned rows) moves a
+// stage with one TMA bulk copy per row into a per-warp shared-memory ring of D stages, each
+// completing on its own mbarrier (one elected lane issues, every lane waits with a bounded
+// poll); the plain path (E = 1) loads directly.
 // ---------------------------------------------------------------------------------------
+constexpr int kSpinLimit = 1 << 20;   // mbarrier polls before a wait gives up (status TIMEOUT)
+
 template <typename DQ, typename DP, int E>
 struct Feed;
 
@@ -136,39 +135,78 @@ template <typename DQ, typename DP>
 struct Feed<DQ, DP, 8> {
     static constexpr int BQ = 8 * (int)sizeof(DQ);
     static constexpr int BP = 8 * (int)sizeof(DP);
-    static constexpr int U = (BQ + BP) <= 32 ? 2 : 1;
-    static constexpr int SUB = 32 * (BQ + BP);               // one chunk of each row, 32 lanes
-    static constexpr int STAGE = U * SUB;
-    static constexpr int D = (kRingBytesPerCta / kWarps / STAGE) < 2 ? 2 : (kRingBytesPerCta / kWarps / STAGE);
-    static constexpr int RING = D * STAGE;                   // bytes per warp
+    static constexpr int U = (2 * 32 * (BQ + BP) <= 2048) ? 2 : 1;
+    static constexpr int GRP = 32 * U;                       // chunks per stage
+    static constexpr int ROWQ = GRP * BQ, ROWP = GRP * BP;
+    static constexpr int STAGE = ROWQ + ROWP;
+    static constexpr int DR = (kRingBytesPerCta / kWarps - 64) / STAGE;
+    static constexpr int D = DR < 2 ? 2 : (DR > 8 ? 8 : DR);
+    static constexpr int RING = D * STAGE + 64;              // bytes per warp (stages + barriers)
     char* base;
+    uint64_t* bar;
     int lane;
-    __device__ __forceinline__ void issue(int slot, const void* rq, const void* rp, int64_t k0, int64_t c1) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t k = k0 + u * 32 + lane;
-            if (k < c1) {
-                char* sq = base + slot * STAGE + u * SUB + lane * BQ;
-                char* sp = base + slot * STAGE + u * SUB + 32 * BQ + lane * BP;
-                if (rq) {
-                    const char* g = reinterpret_cast<const char*>(rq) + k * BQ;
-#pragma unroll
-                    for (int v = 0; v < BQ / 16; ++v) cp_async16(sq + 16 * v, g + 16 * v);
-                }
-                const char* g = reinterpret_cast<const char*>(rp) + k * BP;
-#pragma unroll
-                for (int v = 0; v < BP / 16; ++v) cp_async16(sp + 16 * v, g + 16 * v);
+    unsigned phase;     // parity of the next completion of each slot
+    unsigned pending;   // slots with a stage issued and not yet waited for
+    bool timeout;
+    __device__ __forceinline__ void init(char* b, int ln) {
+        base = b;
+        bar = reinterpret_cast<uint64_t*>(b + D * STAGE);
+        lane = ln;
+        phase = 0;
+        pending = 0;
+        timeout = false;
+        if (lane == 0) {
+            for (int i = 0; i < D; ++i) mbar_init(&bar[i], 1);
+            mbar_init_fence();
+        }
+        __syncwarp();
+    }
+    // segment start of a row (bytes), or null
+    __device__ __forceinline__ const char* seg_q(const void* row, int64_t c0) const {
+        return row ? reinterpret_cast<const char*>(row) + c0 * BQ : nullptr;
+    }
+    __device__ __forceinline__ const char* seg_p(const void* row, int64_t c0) const {
+        return reinterpret_cast<const char*>(row) + c0 * BP;
+    }
+    // stage of chunks [rel, rel + GRP) of the segment (nrel chunks long) into ring slot `slot`
+    __device__ __forceinline__ void issue(int slot, const char* gq, const char* gp, int rel, int nrel) {
+        if (timeout) return;   // after a failed wait nothing new is put in flight
+        pending |= 1u << slot;
+        __syncwarp();          // every lane is done reading this slot's previous stage
+        if (lane == 0) {
+            const int n = min(GRP, nrel - rel);
+            fence_proxy_async_smem();
+            mbar_expect_tx(&bar[slot], (unsigned)(n * ((gq ? BQ : 0) + BP)));
+            if (gq) bulk_g2s(base + slot * STAGE, gq + (size_t)rel * BQ, (unsigned)(n * BQ), &bar[slot]);
+            bulk_g2s(base + slot * STAGE + ROWQ, gp + (size_t)rel * BP, (unsigned)(n * BP), &bar[slot]);
+        }
+    }
+    __device__ __forceinline__ void wait(int slot) {
+        if (timeout) return;
+        const unsigned parity = (phase >> slot) & 1u;
+        int n = 0;
+        while (!mbar_try_wait(&bar[slot], parity)) {
+            if (++n > kSpinLimit) {
+                timeout = true;   // the slot stays pending; drain() waits for it once more
+                return;
             }
         }
-        cp_async_commit();
+        phase ^= 1u << slot;
+        pending &= ~(1u << slot);
     }
-    __device__ __forceinline__ void empty() { cp_async_commit(); }
-    __device__ __forceinline__ void wait() { cp_async_wait<D - 1>(); }
-    __device__ __forceinline__ void drain() { cp_async_wait<0>(); }
+    // before the CTA exits: wait (bounded) for any copy still in flight after a failed wait
+    __device__ __forceinline__ void drain() {
+        for (int slot = 0; slot < D; ++slot) {
+            if (!((pending >> slot) & 1u)) continue;
+            const unsigned parity = (phase >> slot) & 1u;
+            for (int n = 0; n < kSpinLimit && !mbar_try_wait(&bar[slot], parity); ++n) {
+            }
+        }
+    }
     __device__ __forceinline__ void get(int slot, int u, const void*, const void*, int64_t, bool has_q,
                                         float (&xq)[8], float (&xp)[8]) const {
-        const char* sq = base + slot * STAGE + u * SUB + lane * BQ;
-        const char* sp = base + slot * STAGE + u * SUB + 32 * BQ + lane * BP;
+        const char* sq = base + slot * STAGE + (u * 32 + lane) * BQ;
+        const char* sp = base + slot * STAGE + ROWQ + (u * 32 + lane) * BP;
         if (has_q) unpack<DQ>(sq, xq);
         unpack<DP>(sp, xp);
     }
@@ -190,13 +228,19 @@ struct Feed<DQ, DP, 8> {
 template <typename DQ, typename DP>
 struct Feed<DQ, DP, 1> {
     static constexpr int U = 4;
+    static constexpr int GRP = 32 * U;
     static constexpr int D = 1;
     static constexpr int RING = 0;
-    char* base;
     int lane;
-    __device__ __forceinline__ void issue(int, const void*, const void*, int64_t, int64_t) {}
-    __device__ __forceinline__ void empty() {}
-    __device__ __forceinline__ void wait() {}
+    bool timeout;
+    __device__ __forceinline__ void init(char*, int ln) {
+        lane = ln;
+        timeout = false;
+    }
+    __device__ __forceinline__ const char* seg_q(const void*, int64_t) const { return nullptr; }
+    __device__ __forceinline__ const char* seg_p(const void*, int64_t) const { return nullptr; }
+    __device__ __forceinline__ void issue(int, const char*, const char*, int, int) {}
+    __device__ __forceinline__ void wait(int) {}
     __device__ __forceinline__ void drain() {}
     __device__ __forceinline__ void get(int, int, const void* rq, const void* rp, int64_t k, bool has_q,
                                         float (&xq)[1], float (&xp)[1]) const {
@@ -208,23 +252,6 @@ struct Feed<DQ, DP, 1> {
 // ---------------------------------------------------------------------------------------
 // Per-lane accumulators
 // ---------------------------------------------------------------------------------------
-// Pairwise sum of a chunk's E terms (each term takes part in log2(E) roundings).
-template <int E>
-__device__ __forceinline__ float chunk_sum(const float (&t)[E]) {
-    if constexpr (E == 1) {
-        return t[0];
-    } else {
-        float2 v[E / 2];
-#pragma unroll
-        for (int j = 0; j < E / 2; ++j) v[j] = make_float2(t[2 * j], t[2 * j + 1]);
-#pragma unroll
-        for (int w = E / 2; w > 1; w /= 2)
-#pragma unroll
-            for (int j = 0; j < w / 2; ++j) v[j] = fadd2(v[j], v[j + w / 2]);
-        return v[0].x + v[0].y;
-    }
-}
-
 // Kahan-compensated running sum of chunk sums: the true sum is s - c.  Accumulating one
 // float per chunk against a large running total would otherwise lose ~3e-8 of the total per
 // addition when one token dominates the row.
@@ -244,46 +271,50 @@ struct Kahan {
 };
 
 // sum 2^(x a - K) of one lane (T > 0 rows), with the reference K raised only when needed
-template <int E>
 struct LaneSum {
     float K = kNoRef;
     Kahan acc;
 
-    __device__ __forceinline__ float terms(const float (&x)[E], float ah, float al) const {
-        float t[E];
-        if (E == 1) {
-            t[0] = ex2(fmaf(x[0], al, fmaf(x[0], ah, -K)));
+    template <int G>
+    __device__ __forceinline__ float terms(const float (&x)[G], float ah, float al) const {
+        if constexpr (G == 1) {
+            return ex2(fmaf(x[0], al, fmaf(x[0], ah, -K)));
         } else {
             const float2 nk = make_float2(-K, -K), a2h = make_float2(ah, ah), a2l = make_float2(al, al);
+            float2 e[G / 2];
 #pragma unroll
-            for (int j = 0; j < E / 2; ++j) {
-                const float2 xx = make_float2(x[2 * j], x[2 * j + 1]);
-                const float2 e = ffma2(xx, a2l, ffma2(xx, a2h, nk));
-                t[2 * j] = ex2(e.x);
-                t[2 * j + 1] = ex2(e.y);
+            for (int j = 0; j < G / 2; ++j) {
+                const float2 z = ffma2(make_float2(x[2 * j], x[2 * j + 1]), a2l,
+                                       ffma2(make_float2(x[2 * j], x[2 * j + 1]), a2h, nk));
+                e[j] = make_float2(ex2(z.x), ex2(z.y));
+            }
+#pragma unroll
+            for (int w = G / 2; w > 1; w /= 2)
+#pragma unroll
+                for (int j = 0; j < w / 2; ++j) e[j] = fadd2(e[j], e[j + w / 2]);
+            return e[0].x + e[0].y;
+        }
+    }
+    // The fast path keeps every term of the load <= 16, i.e. its exponent x a - K <= 4, where
+    // float32 rounds the exponent to 1.2e-7 (2^e to ~8e-8); a load with a larger sum (a new
+    // maximum more than 4 above K, the first finite load, +inf or NaN) raises K to
+    // ceil(max x a) and is recomputed.
+    template <int G>
+    __device__ __forceinline__ void add(const float (&x)[G], float ah, float al) {
+        float t;
+        for (int pass = 0;; ++pass) {   // one copy of the terms: the retry is rare
+            t = terms<G>(x, ah, al);
+            if (t <= 16.f || pass > 0) break;
+            float vm = x[0];
+#pragma unroll
+            for (int j = 1; j < G; ++j) vm = fmaxf(vm, x[j]);   // NaN-ignoring
+            const float kv = ceilf(vm * ah);
+            if (kv > K) {
+                acc.scale(pow2_int(K - kv));
+                K = kv;
             }
         }
-        return chunk_sum<E>(t);
-    }
-    // The fast path keeps every term of the chunk <= 16, i.e. its exponent x a - K <= 4, where
-    // float32 rounds the exponent to 1.2e-7 (2^e to ~8e-8); a chunk with a larger sum (a new
-    // maximum more than 4 above K, the first finite chunk, +inf or NaN) raises K to
-    // ceil(max x a) and is recomputed.
-    __device__ __forceinline__ void add(const float (&x)[E], float ah, float al) {
-        const float t = terms(x, ah, al);
-        if (t <= 16.f) {
-            acc.add(t);
-            return;
-        }
-        float vm = x[0];
-#pragma unroll
-        for (int j = 1; j < E; ++j) vm = fmaxf(vm, x[j]);   // NaN-ignoring
-        const float kv = ceilf(vm * ah);
-        if (kv > K) {
-            acc.scale(pow2_int(K - kv));
-            K = kv;
-        }
-        acc.add(terms(x, ah, al));                             // NaN / inf stay and poison the row
+        acc.add(t);                     // NaN / inf stay and poison the row
     }
     // warp-combine and publish (lane 0)
     __device__ __forceinline__ void publish(Part* dst, int lane) const {
@@ -299,18 +330,18 @@ struct LaneSum {
 };
 
 // max and its lowest index (T = 0 rows); NaN propagates
-template <int E>
 struct LaneMax {
     float m = -kInf;
     int idx = INT_MAX;
-    __device__ __forceinline__ void add(const float (&x)[E], int64_t elem0) {
+    template <int G>
+    __device__ __forceinline__ void add(const float (&x)[G], int64_t elem0) {
         float vm = x[0];
 #pragma unroll
-        for (int j = 1; j < E; ++j) vm = fmax_nan(vm, x[j]);
+        for (int j = 1; j < G; ++j) vm = fmax_nan(vm, x[j]);
         if (!(vm <= m)) {
             int j0 = 0;
 #pragma unroll
-            for (int j = E - 1; j >= 0; --j)
+            for (int j = G - 1; j >= 0; --j)
                 if (x[j] == vm) j0 = j;
             idx = (int)(elem0 + j0);
             m = fmax_nan(m, vm);
@@ -346,6 +377,42 @@ __device__ __forceinline__ void resid_weights(const float (&xq)[E], const float 
     }
 }
 
+// sum of a chunk's residual weights (pairwise, packed)
+template <int E>
+__device__ __forceinline__ float resid_chunk_sum(const float (&xq)[E], const float (&xp)[E], float Kq, float Kp,
+                                                 float ah, float al, float c) {
+    if constexpr (E == 1) {
+        float w[1];
+        resid_weights<1>(xq, xp, Kq, Kp, ah, al, c, w);
+        return w[0];
+    } else {
+        const float2 a2h = make_float2(ah, ah), a2l = make_float2(al, al);
+        const float2 nkp = make_float2(-Kp, -Kp), nkq = make_float2(-Kq, -Kq);
+        float2 d[E / 2];
+#pragma unroll
+        for (int j = 0; j < E / 2; ++j) {
+            const float2 pp = make_float2(xp[2 * j], xp[2 * j + 1]);
+            const float2 qq = make_float2(xq[2 * j], xq[2 * j + 1]);
+            const float2 e1 = ffma2(pp, a2l, ffma2(pp, a2h, nkp));
+            const float2 e2 = ffma2(qq, a2l, ffma2(qq, a2h, nkq));
+            d[j] = make_float2(fmaxf(0.f, fmaf(c, ex2(e1.x), -ex2(e2.x))), fmaxf(0.f, fmaf(c, ex2(e1.y), -ex2(e2.y))));
+        }
+#pragma unroll
+        for (int w = E / 2; w > 1; w /= 2)
+#pragma unroll
+            for (int j = 0; j < w / 2; ++j) d[j] = fadd2(d[j], d[j + w / 2]);
+        return d[0].x + d[0].y;
+    }
+}
+
+// sum of a chunk's target weights 2^(xp a - Kp) (the bonus slot's distribution)
+template <int E>
+__device__ __forceinline__ float target_chunk_sum(const float (&xp)[E], float Kp, float ah, float al) {
+    LaneSum t;
+    t.K = Kp;
+    return t.terms<E>(xp, ah, al);
+}
+
 // ---------------------------------------------------------------------------------------
 // Warp sweep over this warp's segment [c0, c1) of a list of items (a row or a row pair),
 // each split into groups of U * 32 chunks; the ring runs D - 1 groups ahead of the consumer.
@@ -358,17 +425,23 @@ __device__ __forceinline__ void sweep(Feed<DQ, DP, E>& feed, int items, int64_t 
     constexpr int D = Feed<DQ, DP, E>::D;
     constexpr int U = Feed<DQ, DP, E>::U;
     const int G = (c1 > c0) ? (int)((c1 - c0 + 32 * U - 1) / (32 * U)) : 0;
+    const int nrel = (int)(c1 - c0);
     int ii = 0, gi = 0, slot_i = 0;
-    const void *iq = nullptr, *ip = nullptr;
-    if (G > 0 && items > 0) rows(0, iq, ip);
+    const char *iq = nullptr, *ip = nullptr;
+    auto load_rows = [&](int it) {
+        const void *rq, *rp;
+        rows(it, rq, rp);
+        iq = feed.seg_q(rq, c0);
+        ip = feed.seg_p(rp, c0);
+    };
+    if (G > 0 && items > 0) load_rows(0);
     auto issue_next = [&]() {
-        if (ii < items) feed.issue(slot_i, iq, ip, c0 + (int64_t)gi * 32 * U, c1);
-        else feed.empty();
+        if (ii < items) feed.issue(slot_i, iq, ip, gi * 32 * U, nrel);
         if (++slot_i == D) slot_i = 0;
         if (++gi == G) {
             gi = 0;
             ++ii;
-            if (ii < items) rows(ii, iq, ip);
+            if (ii < items) load_rows(ii);
         }
     };
     if (G > 0)
@@ -380,7 +453,7 @@ __device__ __forceinline__ void sweep(Feed<DQ, DP, E>& feed, int items, int64_t 
         begin_item(it);
         for (int g = 0; g < G; ++g) {
             issue_next();
-            feed.wait();
+            feed.wait(slot_c);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t k = c0 + ((int64_t)g * U + u) * 32 + lane;
@@ -394,7 +467,6 @@ __device__ __forceinline__ void sweep(Feed<DQ, DP, E>& feed, int items, int64_t 
         }
         end_item(it);
     }
-    feed.drain();
 }
 
 // Inverse-CDF rescan of one warp segment in 64-bit fixed point (weights times `scale`): the
@@ -489,8 +561,221 @@ __device__ __forceinline__ float fixed_scale(float wmax) {
     return pow2_int((float)(40 - e));
 }
 
+// stream j breaks the packed layout: its draft count is outside [0, kmax], or cu[0] != 0
+__device__ __forceinline__ bool offsets_bad(const VerifyParams& p, int j) {
+    const int n = p.cu[j + 1] - p.cu[j];
+    return n < 0 || n > p.kmax || (j == 0 && p.cu[0] != 0);
+}
+
+// Streams [0, L) form the valid packed prefix (cu[0] = 0, every count in [0, kmax]); returns
+// L.  Every thread of the block must call it.
+__device__ int valid_prefix(const VerifyParams& p) {
+    __shared__ int first_bad;
+    if (threadIdx.x == 0) first_bad = p.B;
+    __syncthreads();
+    for (int j = threadIdx.x; j < p.B; j += blockDim.x)
+        if (offsets_bad(p, j)) atomicMin(&first_bad, j);
+    __syncthreads();
+    const int L = first_bad;
+    __syncthreads();
+    return L;
+}
+
+// Chunks per warp of the stats kernel: equal shares of all rows' chunks, but at least
+// ceil(n / (kPiecesMax - 2)) so that no row is cut into more than kPiecesMax pieces.
+__device__ __forceinline__ int64_t stats_share(int64_t rows, int64_t n, int64_t nw) {
+    const int64_t lw = (rows * n + nw - 1) / nw;
+    const int64_t lmin = (n + kPiecesMax - 3) / (kPiecesMax - 2);
+    return lw > lmin ? lw : (lmin > 0 ? lmin : 1);
+}
+
 // ---------------------------------------------------------------------------------------
-// The kernel
+// Stats kernel: every logit of the batch is read once.
+//
+// Rows are numbered stream by stream: stream b owns rows [g_b, g_b + 2 N_b + 1), g_b =
+// 2 cu[b] + b; its target rows 0..N_b come first, then its draft rows 0..N_b-1.  The chunks
+// of all these rows, end to end, are cut into equal contiguous shares, one per warp of a
+// persistent grid, so every warp streams the same number of bytes, from one row or a few
+// consecutive ones.  Per row piece a warp leaves one partial: (reference K, sum 2^(l a - K))
+// for T > 0, (max, lowest argmax) for T = 0; the partial of piece k of row rho sits at
+// rho * kPiecesMax + k.  Draft rows of greedy streams and all rows of a stream with an
+// invalid temperature are skipped (never read).
+// ---------------------------------------------------------------------------------------
+template <typename T, int E, typename AddFn>
+__device__ __forceinline__ void stream_piece(const void* row, int64_t c0, int64_t c1, int lane, AddFn add) {
+    constexpr int U = (E == 8) ? (sizeof(T) == 2 ? 4 : 2) : 8;   // 64 bytes per lane and batch
+    constexpr int G = 32 * U;
+    Chunk<T, E> a[U], b[U];
+    auto load = [&](Chunk<T, E>(&v)[U], int64_t base) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = base + u * 32 + lane;
+            if (k < c1) v[u].load(row, k);
+        }
+    };
+    auto consume = [&](const Chunk<T, E>(&v)[U], int64_t base) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = base + u * 32 + lane;
+            if (k < c1) {
+                float x[E];
+                v[u].unpack(x);
+                add(x, k * E);
+            }
+        }
+    };
+    // two register buffers: the next batch is in flight while the current one is summed
+    load(a, c0);
+    for (int64_t k = c0; k < c1; k += 2 * G) {
+        if (k + G < c1) load(b, k + G);
+        consume(a, k);
+        if (k + G >= c1) break;
+        if (k + 2 * G < c1) load(a, k + 2 * G);
+        consume(b, k + G);
+    }
+}
+
+// 16-byte rows (E = 8): each lane copies its own chunks into a per-warp ring of kStages
+// stages of 2 KB with cp.async and later reads back only those chunks, so the ring needs no
+// synchronisation beyond each thread's own wait_group; kStages - 1 stages are in flight while
+// one is summed.  A float32 chunk (32 bytes) is stored as two 16-byte planes.
+constexpr int kStages = 4;
+constexpr int kStageBytes = 2048;
+constexpr int kStatsRingBytes = kWarps * kStages * kStageBytes;
+static size_t stats_smem_bytes(int E) { return E == 8 ? (size_t)kStatsRingBytes : 0; }
+
+template <typename T, typename AddFn>
+__device__ __forceinline__ void stream_piece_ring(char* ring, const void* row, int64_t c0, int64_t c1, int lane,
+                                                  AddFn add) {
+    constexpr int BT = 8 * (int)sizeof(T);   // bytes per chunk
+    constexpr int G = kStageBytes / BT;      // chunks per stage
+    constexpr int U = G / 32;                // chunks per lane and stage
+    constexpr int LPC = BT / 16;             // 16-byte copies per chunk
+    const char* g = reinterpret_cast<const char*>(row);
+    const int64_t nb = (c1 - c0 + G - 1) / G;
+    auto issue = [&](int64_t i, int slot) {
+        if (i < nb) {
+            char* st = ring + slot * kStageBytes;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t k = c0 + i * G + u * 32 + lane;
+                if (k < c1)
+#pragma unroll
+                    for (int l = 0; l < LPC; ++l) cp_async16(st + l * (G * 16) + (u * 32 + lane) * 16, g + k * BT + 16 * l);
+            }
+        }
+        cp_async_commit();   // an empty group keeps the group count in step
+    };
+#pragma unroll
+    for (int i = 0; i < kStages - 1; ++i) issue(i, i);
+    int slot = 0;
+    for (int64_t i = 0; i < nb; ++i) {
+        issue(i + kStages - 1, slot == 0 ? kStages - 1 : slot - 1);
+        cp_async_wait<kStages - 1>();
+        const char* st = ring + slot * kStageBytes;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = c0 + i * G + u * 32 + lane;
+            if (k < c1) {
+                float x[8];
+                if constexpr (sizeof(T) == 2) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(st + (u * 32 + lane) * 16);
+                    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+                    x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+                } else {
+                    const float4 a = *reinterpret_cast<const float4*>(st + (u * 32 + lane) * 16);
+                    const float4 b = *reinterpret_cast<const float4*>(st + G * 16 + (u * 32 + lane) * 16);
+                    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+                }
+                add(x, k * 8);
+            }
+        }
+        slot = (slot + 1 == kStages) ? 0 : slot + 1;
+    }
+}
+
+template <typename T, int E>
+__device__ __forceinline__ void stats_piece(char* ring, const void* row, int64_t c0, int64_t c1, bool greedy,
+                                            float ah, float al, int lane, Part* dst) {
+    if (greedy) {
+        LaneMax mx;
+        auto f = [&](const float (&x)[E], int64_t e0) { mx.add<E>(x, e0); };
+        if constexpr (E == 8) stream_piece_ring<T>(ring, row, c0, c1, lane, f);
+        else stream_piece<T, E>(row, c0, c1, lane, f);
+        mx.publish(dst, lane);
+    } else {
+        LaneSum sum;
+        auto f = [&](const float (&x)[E], int64_t) { sum.add<E>(x, ah, al); };
+        if constexpr (E == 8) stream_piece_ring<T>(ring, row, c0, c1, lane, f);
+        else stream_piece<T, E>(row, c0, c1, lane, f);
+        sum.publish(dst, lane);
+    }
+}
+
+template <typename DQ, typename DP, int E>
+__global__ void __launch_bounds__(kThreads, 3) stats_kernel(const VerifyParams p) {
+    extern __shared__ __align__(16) char stats_smem[];
+    const int lane = threadIdx.x & 31;
+    char* ring = stats_smem + (threadIdx.x >> 5) * (kStages * kStageBytes);
+    const int L = valid_prefix(p);
+    if (L == 0) return;
+    const int64_t n = p.nchunk;
+    const int64_t rows = 2 * (int64_t)p.cu[L] + L;
+    const int64_t lw = stats_share(rows, n, p.stats_warps);
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    int64_t f = gw * lw;
+    const int64_t f1 = min(f + lw, rows * n);
+    if (f >= f1) return;
+    int64_t rho = f / n;
+    int64_t c = f - rho * n;
+    // the stream of the first row: largest b in [0, L) with g_b <= rho
+    int lo = 0, hi = L - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (2 * (int64_t)p.cu[mid] + mid <= rho) lo = mid;
+        else hi = mid - 1;
+    }
+    int b = lo;
+    int64_t gb = 2 * (int64_t)p.cu[b] + b;
+    int Nb = p.cu[b + 1] - p.cu[b];
+    const int64_t V = p.V;
+    while (f < f1) {
+        const int64_t c_end = min(n, c + (f1 - f));
+        while (rho - gb > 2 * (int64_t)Nb) {
+            ++b;
+            gb = 2 * (int64_t)p.cu[b] + b;
+            Nb = p.cu[b + 1] - p.cu[b];
+        }
+        const int64_t j = rho - gb;
+        const float T = p.temp[b];
+        const bool greedy = (T == 0.f);
+        const bool draft = j > Nb;
+        const bool skip = !(isfinite(T) && (T == 0.f || T >= FLT_MIN)) || (draft && greedy);
+        if (!skip) {
+            float ah = 0.f, al = 0.f;
+            if (!greedy) {
+                const df l2e{1.4426950216293335f, 1.925963033500011e-08f};
+                const df a = df_div(l2e, df_make(T));
+                ah = a.hi;
+                al = a.lo;
+            }
+            Part* dst = p.part + rho * kPiecesMax + (gw - rho * n / lw);
+            if (draft)
+                stats_piece<DQ, E>(ring, row_ptr<DQ>(p.dq, (int64_t)p.cu[b] + (j - Nb - 1), V), c, c_end, false,
+                                   ah, al, lane, dst);
+            else
+                stats_piece<DP, E>(ring, row_ptr<DP>(p.dp, (int64_t)p.cu[b] + b + j, V), c, c_end, greedy, ah, al,
+                                   lane, dst);
+        }
+        f += c_end - c;
+        c = 0;
+        ++rho;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// The verify kernel (one cluster per stream)
 // ---------------------------------------------------------------------------------------
 template <typename DQ, typename DP, int E>
 __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams p) {
@@ -506,14 +791,14 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     const int64_t c1 = min(p.nchunk, c0 + p.seg_chunks);
     const int64_t V = p.V;
     Feed<DQ, DP, E> feed;
-    feed.base = ring_smem + warp * Feed<DQ, DP, E>::RING;
-    feed.lane = lane;
+    feed.init(ring_smem + warp * Feed<DQ, DP, E>::RING, lane);
 
     // ---- stream header (identical in every CTA): offsets, temperature, tokens, and the draft
     // and target logits at each draft token (loaded now, consumed after the sweep)
     const int base = p.cu[b];
     const int n_raw = p.cu[b + 1] - base;
-    const bool offsets_ok = n_raw >= 0 && n_raw <= p.kmax;
+    const int Lv = valid_prefix(p);   // streams from the first broken count on are invalid
+    const bool offsets_ok = b < Lv;
     const int N = offsets_ok ? n_raw : 0;
     const float T = p.temp[b];
     const bool temp_ok = isfinite(T) && (T == 0.f || T >= FLT_MIN);
@@ -522,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     const int64_t tbase = dbase + b;
     auto qrow = [&](int i) { return row_ptr<DQ>(p.dq, dbase + i, V); };
     auto prow = [&](int i) { return row_ptr<DP>(p.dp, tbase + i, V); };
+    if (tid < kWarps) sh.to_flag[tid] = 0;
     bool bad_tok = false;
     if (offsets_ok && temp_ok && tid < N) {
         const int xi = p.tokens[base + tid];
@@ -560,56 +846,21 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     const int nrows = 2 * N + 1;   // part index: draft row i -> i, target row i -> N + i
 
     if (sh.status == SPEC_ST_OK) {
-        // ---- one sweep over every row of the stream
-        if (!greedy) {
-            // items: 0 = bonus row N alone, 1..N-1 = pairs 1..N-1, N = pair 0
-            auto slot_of = [&](int it) { return it == 0 ? N : (it < N ? it : 0); };
-            LaneSum<E> aq, ap;
-            bool has_q = false;
-            sweep<DQ, DP, E>(
-                feed, N + 1, c0, c1, lane,
-                [&](int it, const void*& rq, const void*& rp) {
-                    const int i = slot_of(it);
-                    rq = (it == 0) ? nullptr : qrow(i);
-                    rp = prow(i);
-                },
-                [&](int it) { has_q = (it != 0); },
-                [&](int64_t, const float (&xq)[E], const float (&xp)[E]) {
-                    if (has_q) aq.add(xq, ah, al);
-                    ap.add(xp, ah, al);
-                },
-                [&](int it) {
-                    const int i = slot_of(it);
-                    if (it != 0) aq.publish(&sh.part[i][warp], lane);
-                    ap.publish(&sh.part[N + i][warp], lane);
-                    aq = LaneSum<E>();
-                    ap = LaneSum<E>();
-                });
-        } else {
-            LaneMax<E> am;
-            sweep<DQ, DP, E>(
-                feed, N + 1, c0, c1, lane,
-                [&](int it, const void*& rq, const void*& rp) {
-                    rq = nullptr;
-                    rp = prow(it);
-                },
-                [&](int) {},
-                [&](int64_t k, const float (&)[E], const float (&xp)[E]) { am.add(xp, k * E); },
-                [&](int it) {
-                    am.publish(&sh.part[N + it][warp], lane);
-                    am = LaneMax<E>();
-                });
-        }
-        cluster_sync_all();
-
-        // ---- cluster reduction of the per-segment partials (same order in every CTA)
+        // ---- row statistics from the stats kernel's per-segment partials (same order in
+        // every CTA, so every CTA holds bit-identical values)
+        const int64_t n = p.nchunk;
+        const int64_t lw = stats_share(2 * (int64_t)p.cu[Lv] + Lv, n, p.stats_warps);
         for (int r = (greedy ? N : 0) + warp; r < nrows; r += kWarps) {
+            // stats row: target row i at g_b + i, draft row i at g_b + N + 1 + i
+            const int64_t rho = 2 * (int64_t)base + b + (r < N ? N + 1 + r : r - N);
+            const int64_t first = rho * n / lw;
+            const int cnt = (int)((rho * n + n - 1) / lw - first) + 1;   // pieces of this row
             Part e[2];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-                const int s = lane + 32 * k;
-                if (s < nseg)
-                    e[k] = *cluster.map_shared_rank(&sh.part[r][s % kWarps], s / kWarps);
+                const int pk = lane + 32 * k;
+                if (pk < cnt)
+                    e[k] = p.part[rho * kPiecesMax + pk];
                 else
                     e[k] = Part{greedy ? -kInf : kNoRef, 0.f, 0.f, INT_MAX};
             }
@@ -625,13 +876,10 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
             }
             const float Kr = warp_max(fmaxf(e[0].K, e[1].K));
             df z{0.f, 0.f};
-            float segw[2];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const float sc = (e[k].K == Kr) ? 1.f : pow2_int(e[k].K - Kr);
-                const df v = df_scale(df{e[k].s_hi, e[k].s_lo}, sc);
-                segw[k] = df_to_f(v);
-                z = df_add(z, v);
+                z = df_add(z, df_scale(df{e[k].s_hi, e[k].s_lo}, sc));
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -642,11 +890,6 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
                 sh.rowK[r] = Kr;
                 sh.rowZ[r] = z;
                 sh.rowArg[r] = INT_MAX;
-            }
-            if (r == 2 * N) {
-#pragma unroll
-                for (int k = 0; k < 2; ++k)
-                    if (lane + 32 * k < nseg) sh.bonus_w[lane + 32 * k] = segw[k];
             }
         }
         __syncthreads();
@@ -729,11 +972,17 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
                     sh.pass_list[n++] = tau;
                 }
             }
+            if (sh.tau == N) {   // every draft accepted: the sweep sums the bonus row instead
+                sh.pass_list[0] = N;
+                n = 1;
+                sh.sample_bonus = 1;
+            }
             sh.n_pass = n;
         }
         __syncthreads();
         np = sh.n_pass;
-        if (tid < np) {
+        const bool bonus_sweep = sh.sample_bonus != 0;
+        if (tid < np && !bonus_sweep) {
             const int i = sh.pass_list[tid];
             sh.cval[i] = df_to_f(df_div(df_mul(sh.w[i], sh.rowZ[i]), sh.rowZ[N + i]));
         }
@@ -747,20 +996,19 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
                 feed, np, c0, c1, lane,
                 [&](int it, const void*& rq, const void*& rp) {
                     const int i = sh.pass_list[it];
-                    rq = qrow(i);
+                    rq = bonus_sweep ? nullptr : qrow(i);
                     rp = prow(i);
                 },
                 [&](int it) {
                     const int i = sh.pass_list[it];
-                    Kq = sh.rowK[i];
+                    Kq = bonus_sweep ? 0.f : sh.rowK[i];
                     Kp = sh.rowK[N + i];
-                    cc = sh.cval[i];
+                    cc = bonus_sweep ? 1.f : sh.cval[i];
                     acc = Kahan();
                 },
                 [&](int64_t, const float (&xq)[E], const float (&xp)[E]) {
-                    float w[E];
-                    resid_weights<E>(xq, xp, Kq, Kp, ah, al, cc, w);
-                    acc.add(chunk_sum<E>(w));
+                    if (bonus_sweep) acc.add(target_chunk_sum<E>(xp, Kp, ah, al));
+                    else acc.add(resid_chunk_sum<E>(xq, xp, Kq, Kp, ah, al, cc));
                 },
                 [&](int it) {
                     df tot = acc.value();
@@ -771,9 +1019,16 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
                     }
                     if (lane == 0) sh.res_part[it][warp] = df_to_f(tot);
                 });
+            if (lane == 0 && feed.timeout) sh.to_flag[warp] = 1;
             cluster_sync_all();
+            {
+                bool to = false;
+                if (tid < nseg) to = *cluster.map_shared_rank(&sh.to_flag[tid % kWarps], tid / kWarps) != 0;
+                to = __syncthreads_or(to);
+                if (to && tid == 0) sh.status = SPEC_ST_TIMEOUT;
+            }
             // per pass item: r_i = (sum over all segments) / Z_q
-            for (int it = warp; it < np; it += kWarps) {
+            for (int it = warp; it < np && !bonus_sweep; it += kWarps) {
                 df tot{0.f, 0.f};
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
@@ -819,14 +1074,9 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
             for (int it = 0; it < np; ++it)
                 if (sh.pass_list[it] == tau) item = it;
             float w0 = 0.f, w1 = 0.f;
-            if (bonus) {
-                if (lane < nseg) w0 = sh.bonus_w[lane];
-                if (lane + 32 < nseg) w1 = sh.bonus_w[lane + 32];
-            } else {
-                if (lane < nseg) w0 = *cluster.map_shared_rank(&sh.res_part[item][lane % kWarps], lane / kWarps);
-                if (lane + 32 < nseg)
-                    w1 = *cluster.map_shared_rank(&sh.res_part[item][(lane + 32) % kWarps], (lane + 32) / kWarps);
-            }
+            if (lane < nseg) w0 = *cluster.map_shared_rank(&sh.res_part[item][lane % kWarps], lane / kWarps);
+            if (lane + 32 < nseg)
+                w1 = *cluster.map_shared_rank(&sh.res_part[item][(lane + 32) % kWarps], (lane + 32) / kWarps);
             const float wmax = warp_max(fmaxf(w0, w1));
             const bool ok = isfinite(wmax) && wmax > 0.f;
             const float scale = ok ? fixed_scale(wmax) : 0.f;
@@ -874,7 +1124,8 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     // every distributed-shared-memory read of this CTA is done: arrive now, wait at the end
     cluster_arrive();
 
-    if (sh.status == SPEC_ST_OK && !greedy && sh.sample_seg == crank * kWarps + warp) {
+    const bool owner = (sh.sample_seg == crank * kWarps + warp);
+    if (sh.status == SPEC_ST_OK && !greedy && sh.sample_seg >= 0 && owner) {
         const int tau = sh.tau;
         int y;
         if (sh.sample_bonus) {
@@ -937,6 +1188,8 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
             }
         }
     }
+    // no TMA copy of this warp may still be writing its ring when the CTA leaves
+    feed.drain();
     // no CTA may leave while another can still read its shared memory
     cluster_wait();
 }
@@ -983,8 +1236,11 @@ static cudaError_t prepare_kernel() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
     if (done[dev]) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(verify_kernel<DQ, DP, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)ring_bytes<DQ, DP, E>());
+    cudaError_t e = cudaFuncSetAttribute(verify_kernel<DQ, DP, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)ring_bytes<DQ, DP, E>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(stats_kernel<DQ, DP, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)stats_smem_bytes(E));
     if (e == cudaSuccess) done[dev] = 1;
     return e;
 }
@@ -1030,6 +1286,26 @@ static int pick_cluster(int B, int64_t nchunk) {
     return best;
 }
 
+// Persistent grid of the stats kernel: every SM filled to its occupancy.
+template <typename DQ, typename DP, int E>
+static int stats_grid() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    if (cache[dev] == 0) {
+        int sms = 0, occ = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, stats_kernel<DQ, DP, E>, kThreads,
+                                                          stats_smem_bytes(E)) != cudaSuccess ||
+            occ < 1) {
+            cudaGetLastError();
+            occ = 1;
+        }
+        cache[dev] = sms * occ;
+    }
+    return cache[dev];
+}
+
 template <typename DQ, typename DP, int E>
 static cudaError_t run_verify(VerifyParams& p, cudaStream_t s, int* info) {
     cudaError_t e = prepare_kernel<DQ, DP, E>();
@@ -1041,6 +1317,11 @@ static cudaError_t run_verify(VerifyParams& p, cudaStream_t s, int* info) {
         info[1] = resident_clusters<DQ, DP, E>(C);
         return cudaSuccess;
     }
+    const int grid = stats_grid<DQ, DP, E>();
+    p.stats_warps = (int64_t)grid * kWarps;
+    stats_kernel<DQ, DP, E><<<grid, kThreads, stats_smem_bytes(E), s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = make_config<DQ, DP, E>(p.B * C, C, s, attr);
     return cudaLaunchKernelEx(&cfg, verify_kernel<DQ, DP, E>, p);
@@ -1091,6 +1372,13 @@ static int verify_entry(const spec_verify_args* a, void* stream, int rule, const
     const bool aligned = (a->V % 8 == 0) && ((uintptr_t)a->target_logits % 16 == 0) &&
                          ((uintptr_t)a->draft_logits % 16 == 0);
     p.nchunk = aligned ? a->V / 8 : a->V;
+    p.part = reinterpret_cast<Part*>(a->workspace);
+    if (info == nullptr) {
+        const size_t need = workspace_bytes(a->B, a->kmax);
+        if (a->workspace == nullptr || a->workspace_bytes < need || (uintptr_t)a->workspace % 16 != 0)
+            return set_error(SPEC_ERR_WORKSPACE, "%s: workspace needs %zu bytes, 16-byte aligned (got %zu)", name,
+                             need, a->workspace_bytes);
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const cudaError_t e = aligned ? dispatch_dtypes<8>(p, a->draft_dtype, a->target_dtype, s, info)
                                   : dispatch_dtypes<1>(p, a->draft_dtype, a->target_dtype, s, info);
@@ -1107,6 +1395,11 @@ extern "C" int spec_verify_tokenwise(const spec_verify_args* args, void* stream)
 
 extern "C" int spec_verify_block(const spec_verify_args* args, void* stream) {
     return sv::verify_entry(args, stream, 1, "spec_verify_block", nullptr);
+}
+
+extern "C" size_t spec_verify_workspace_bytes(int32_t B, int32_t kmax) {
+    if (B < 0 || kmax < 0 || kmax > SPEC_MAX_KMAX) return 0;
+    return sv::workspace_bytes(B, kmax);
 }
 
 extern "C" int spec_verify_launch_info(const spec_verify_args* args, int32_t* cluster_size,

@@ -80,4 +80,24 @@ def test_verify_args_layout_matches_the_header():
     offs = {f[0]: getattr(sv.VerifyArgs, f[0]).offset for f in sv.VerifyArgs._fields_}
     assert offs["cu_drafts"] == 16 and offs["draft_logits"] == 24 and offs["draft_dtype"] == 32
     assert offs["target_logits"] == 40 and offs["seed"] == 72 and offs["diag"] == 120
-    assert ctypes.sizeof(sv.VerifyArgs) == 128
+    assert offs["workspace"] == 128 and offs["workspace_bytes"] == 136
+    assert ctypes.sizeof(sv.VerifyArgs) == 144
+
+
+def test_workspace_size_and_check(L):
+    # one 16-byte partial per (row, stats segment <= 64); a stream has <= 2 kmax + 1 rows
+    assert sv.spec_verify_workspace_bytes(64, 5) == 64 * 11 * 64 * 16
+    assert sv.spec_verify_workspace_bytes(0, 5) == 0
+    assert sv.spec_verify_workspace_bytes(-1, 5) == 0
+    assert sv.spec_verify_workspace_bytes(4, 33) == 0
+    a = sv.VerifyArgs()
+    a.B, a.V, a.kmax = 2, 16, 3
+    for f in ("cu_drafts", "draft_logits", "target_logits", "draft_tokens", "temperature",
+              "accepted_len", "out_tokens", "n_emitted", "status"):
+        setattr(a, f, 4096)                     # never dereferenced: the check comes first
+    assert L.spec_verify_block(ctypes.byref(a), None) == -6
+    assert b"workspace" in L.spec_last_error()
+    a.workspace, a.workspace_bytes = 4096, sv.spec_verify_workspace_bytes(2, 3) - 1
+    assert L.spec_verify_tokenwise(ctypes.byref(a), None) == -6
+    a.workspace, a.workspace_bytes = 4104, 1 << 20   # not 16-byte aligned
+    assert L.spec_verify_block(ctypes.byref(a), None) == -6

@@ -150,6 +150,15 @@ def test_bad_offsets(rule):
     g = run_gpu(rule, d, 2, 0, 0, diag=False)
     assert list(g["status"]) == [0, 5, 5]
     assert (g["out_tokens"][1:] == -1).all()
+    # a stream with a valid count after a broken one, and a batch not starting at row 0
+    for cu, want in (([0, 1, 5, 6], [0, 5, 5]), ([1, 2, 3, 4], [5, 5, 5]), ([0, 1, 3, 4], None)):
+        d["cu"] = torch.tensor(cu, dtype=torch.int32, device="cuda")
+        g = run_gpu(rule, d, 2, 0, 0, diag=False)
+        o = run_oracle(rule, dict(inp, cu_drafts=np.array(cu, np.int32), kmax=2), 0, 0)
+        assert list(g["status"]) == list(o["status"])
+        assert want is None or list(g["status"]) == want
+        ok = (o["status"] == 0) & ~o["tie"]
+        assert (g["accepted_len"][ok] == o["accepted_len"][ok]).all()
 
 
 @pytest.mark.parametrize("rule", ["tokenwise", "block"])
