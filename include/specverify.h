@@ -183,6 +183,22 @@ int spec_verify_tokenwise(const spec_verify_args* args, void* stream);
 int spec_verify_block(const spec_verify_args* args, void* stream);
 
 /*
+ * spec_verify_block_static - spec_verify_block without a caller workspace: the stats partials
+ * go to a fixed device array of 8 MiB that the library reserves when it is loaded, so the
+ * call allocates no memory at all (for callers that cannot allocate device memory where they
+ * verify).  It is an engineering variant of the block verification above; the pages that
+ * define the method have no counterpart to it.
+ * args->workspace and args->workspace_bytes are ignored.  Capacity: B (2 kmax + 1) <= 8192
+ * rows (e.g. B = 256 at kmax = 15); a larger batch returns SPEC_ERR_WORKSPACE and launches
+ * nothing.  The array needs no initial contents.  Every call on a device shares it: calls that
+ * can overlap in time (different streams or host threads) race on it, so the caller must
+ * order them.  The first call on each device looks the array's address up
+ * (cudaGetSymbolAddress); make that first call outside any stream capture.
+ * Errors: as spec_verify_block, plus SPEC_ERR_WORKSPACE for a batch above the capacity.
+ */
+int spec_verify_block_static(const spec_verify_args* args, void* stream);
+
+/*
  * spec_verify_launch_info - the launch configuration a verify call with these arguments
  * would use (no launch, no device data read; only the scalar fields and the two logit
  * pointers' alignment are examined).  cluster_size: CTAs per stream; resident_clusters: how

@@ -23,7 +23,7 @@ import os
 __all__ = [
     "dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block", "adaptive_pick_k",
     "spec_philox_uniforms", "spec_verify_launch_info",
-    "spec_verify_workspace_bytes", "lib", "lib_path", "SpecError",
+    "spec_verify_workspace_bytes", "spec_verify_block_static", "lib", "lib_path", "SpecError",
     "DTYPE_F32", "DTYPE_BF16", "STATUS_NAMES", "DIAG_COLS",
 ]
 
@@ -34,7 +34,7 @@ STATUS_NAMES = {0: "OK", 1: "BAD_TEMPERATURE", 2: "BAD_TOKEN", 3: "BAD_ROW",
                 4: "ZERO_DRAFT_PROB", 5: "BAD_OFFSETS", 6: "TIMEOUT", 7: "NUMERIC"}
 EXPORTED = ["dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block",
             "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info",
-            "spec_verify_workspace_bytes",
+            "spec_verify_workspace_bytes", "spec_verify_block_static",
             "spec_last_error", "spec_version"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -83,6 +83,7 @@ def lib():
     L.dspark_markov_bias.argtypes = [vp, i32, i32, i32, vp, vp, vp, i32, i32, vp, vp]
     L.spec_verify_tokenwise.argtypes = [ctypes.POINTER(VerifyArgs), vp]
     L.spec_verify_block.argtypes = [ctypes.POINTER(VerifyArgs), vp]
+    L.spec_verify_block_static.argtypes = [ctypes.POINTER(VerifyArgs), vp]
     L.adaptive_pick_k.argtypes = [vp, vp, i32, ctypes.c_float, i32, i32, i32, vp, i32, i32,
                                   vp, vp, vp, vp, vp]
     L.spec_philox_uniforms.argtypes = [u64, u64, i32, i32, vp, vp]
@@ -92,7 +93,7 @@ def lib():
     L.spec_verify_workspace_bytes.restype = ctypes.c_size_t
     L.spec_last_error.restype = ctypes.c_char_p
     L.spec_version.restype = ctypes.c_int32
-    for name in ("dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block",
+    for name in ("dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block", "spec_verify_block_static",
                  "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -166,7 +167,7 @@ def dspark_markov_bias(draft_logits, prev_tokens, W1, W2, out=None, stream=None)
 
 
 def _verify(fn, cu_drafts, draft_logits, target_logits, draft_tokens, temperature, kmax, seed,
-            step, out=None, diag=False, stream=None):
+            step, out=None, diag=False, stream=None, workspace=True):
     torch = _torch()
     _dev(cu_drafts, "cu_drafts", torch.int32)
     _dev(target_logits, "target_logits")
@@ -190,10 +191,12 @@ def _verify(fn, cu_drafts, draft_logits, target_logits, draft_tokens, temperatur
         if diag:
             out["diag"] = torch.empty((target_logits.shape[0], DIAG_COLS), dtype=torch.float32,
                                       device=dev)
-    need = spec_verify_workspace_bytes(B, kmax)
-    ws = out.get("workspace")
-    if ws is None or ws.numel() < need:
-        ws = out["workspace"] = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    ws = None
+    if workspace:
+        need = spec_verify_workspace_bytes(B, kmax)
+        ws = out.get("workspace")
+        if ws is None or ws.numel() < need:
+            ws = out["workspace"] = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     a = VerifyArgs()
     a.B, a.V, a.kmax = B, V, kmax
     a.cu_drafts = cu_drafts.data_ptr()
@@ -210,8 +213,8 @@ def _verify(fn, cu_drafts, draft_logits, target_logits, draft_tokens, temperatur
     a.n_emitted = out["n_emitted"].data_ptr()
     a.status = out["status"].data_ptr()
     a.diag = out["diag"].data_ptr() if out.get("diag") is not None else None
-    a.workspace = ws.data_ptr()
-    a.workspace_bytes = ws.numel()
+    a.workspace = ws.data_ptr() if ws is not None else None
+    a.workspace_bytes = ws.numel() if ws is not None else 0
     _check(fn(ctypes.byref(a), _stream(stream)))
     return out
 
@@ -228,6 +231,14 @@ def spec_verify_block(cu_drafts, draft_logits, target_logits, draft_tokens, temp
     """Block verification (see include/specverify.h)."""
     return _verify(lib().spec_verify_block, cu_drafts, draft_logits, target_logits,
                    draft_tokens, temperature, kmax, seed, step, out, diag, stream)
+
+
+def spec_verify_block_static(cu_drafts, draft_logits, target_logits, draft_tokens, temperature,
+                             kmax, seed, step, out=None, diag=False, stream=None):
+    """Block verification on the library's fixed device workspace: no workspace is allocated
+    or passed (see include/specverify.h for its capacity and ordering rule)."""
+    return _verify(lib().spec_verify_block_static, cu_drafts, draft_logits, target_logits,
+                   draft_tokens, temperature, kmax, seed, step, out, diag, stream, workspace=False)
 
 
 def adaptive_pick_k(hidden, w, bias, verify_ms, mode=0, out=None, stream=None):

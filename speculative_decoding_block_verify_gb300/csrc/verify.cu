@@ -1397,6 +1397,60 @@ extern "C" int spec_verify_block(const spec_verify_args* args, void* stream) {
     return sv::verify_entry(args, stream, 1, "spec_verify_block", nullptr);
 }
 
+// ---------------------------------------------------------------------------------------
+// Block verification with a fixed, device-resident workspace.  Some callers cannot allocate
+// device memory at the point where they verify (an allocator that is not theirs to touch, a
+// memory budget fixed at start-up); for them the stats partials live in one array reserved
+// when the library's module is loaded, so this call allocates nothing.  The array holds
+// kStaticWorkspaceBytes: rows B (2 kmax + 1) of kPiecesMax 16-byte partials each, i.e. up to
+// 8192 rows (for example B = 256 at kmax = 15); larger batches are refused.  Its contents need
+// no initial value (every partial a call reads is written by that call's stats kernel).  All
+// calls share the one array, so calls that may overlap in time (different streams, threads)
+// race on it and must be ordered by the caller.
+// ---------------------------------------------------------------------------------------
+namespace sv {
+constexpr size_t kStaticWorkspaceBytes = (size_t)8 << 20;
+static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
+
+// device address of g_static_workspace on the current device, looked up once per device
+static cudaError_t static_workspace(void** ptr) {
+    static void* addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (addr[dev] == nullptr) {
+        void* a = nullptr;
+        e = cudaGetSymbolAddress(&a, g_static_workspace);
+        if (e != cudaSuccess) return e;
+        addr[dev] = a;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
+}
+}  // namespace sv
+
+extern "C" int spec_verify_block_static(const spec_verify_args* args, void* stream) {
+    const char* name = "spec_verify_block_static";
+    if (args == nullptr) return sv::set_error(SPEC_ERR_ARG, "%s: args is NULL", name);
+    spec_verify_args a = *args;
+    const bool shape_ok = a.B >= 0 && a.kmax >= 0 && a.kmax <= SPEC_MAX_KMAX;
+    if (shape_ok && a.B > 0) {   // bad shapes and empty batches are reported by the common path
+        const size_t need = sv::workspace_bytes(a.B, a.kmax);
+        if (need > sv::kStaticWorkspaceBytes)
+            return sv::set_error(SPEC_ERR_WORKSPACE,
+                                 "%s: B = %d, kmax = %d needs %zu workspace bytes; the static workspace "
+                                 "holds %zu (use spec_verify_block with a caller workspace)",
+                                 name, a.B, a.kmax, need, sv::kStaticWorkspaceBytes);
+        void* ws = nullptr;
+        const cudaError_t e = sv::static_workspace(&ws);
+        if (e != cudaSuccess) return sv::set_cuda_error(e, name);
+        a.workspace = ws;
+        a.workspace_bytes = sv::kStaticWorkspaceBytes;
+    }
+    return sv::verify_entry(&a, stream, 1, name, nullptr);
+}
+
 extern "C" size_t spec_verify_workspace_bytes(int32_t B, int32_t kmax) {
     if (B < 0 || kmax < 0 || kmax > SPEC_MAX_KMAX) return 0;
     return sv::workspace_bytes(B, kmax);
