@@ -316,6 +316,37 @@ struct LaneSum {
         }
         acc.add(t);                     // NaN / inf stay and poison the row
     }
+    // A group of U full chunks (x[u] = chunk u of this lane).  The group's maximum comes first,
+    // the reference is raised at most once, and then all 8 U terms are independent: they are
+    // summed as packed pairs and enter the Kahan sum once.  Every term stays <= 16 (exponent
+    // <= 4), as in the per-chunk form, but without a data-dependent branch per chunk.
+    template <int U>
+    __device__ __forceinline__ void add_group(const float (&x)[U][8], float ah, float al) {
+        float m = -kInf;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) m = fmax_nan(m, fmax_nan(x[u][j], x[u][j + 1]));
+        if (!(m * ah <= K + 4.f)) {   // a new maximum (or NaN, which then poisons the sum)
+            const float kv = ceilf(m * ah);
+            if (kv > K) {
+                acc.scale(pow2_int(K - kv));
+                K = kv;
+            }
+        }
+        const float2 nk = make_float2(-K, -K), a2h = make_float2(ah, ah), a2l = make_float2(al, al);
+        float2 s4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 xx = make_float2(x[u][2 * j], x[u][2 * j + 1]);
+                const float2 z = ffma2(xx, a2l, ffma2(xx, a2h, nk));
+                s4[j] = fadd2(s4[j], make_float2(ex2(z.x), ex2(z.y)));
+            }
+        const float2 t = fadd2(fadd2(s4[0], s4[1]), fadd2(s4[2], s4[3]));
+        acc.add(t.x + t.y);
+    }
     // warp-combine and publish (lane 0)
     __device__ __forceinline__ void publish(Part* dst, int lane) const {
         const float Kw = warp_max(K);
@@ -419,9 +450,11 @@ __device__ __forceinline__ float target_chunk_sum(const float (&xp)[E], float Kp
 // rows(it, rq, rp) gives an item's rows; begin(it) / consume(k, xq, xp) / end(it) see the
 // items in order.
 // ---------------------------------------------------------------------------------------
-template <typename DQ, typename DP, int E, typename RowsFn, typename BeginFn, typename ConsumeFn, typename EndFn>
+template <typename DQ, typename DP, int E, typename RowsFn, typename BeginFn, typename ConsumeFn, typename EndFn,
+          typename FlushFn>
 __device__ __forceinline__ void sweep(Feed<DQ, DP, E>& feed, int items, int64_t c0, int64_t c1, int lane,
-                                      RowsFn rows, BeginFn begin_item, ConsumeFn consume, EndFn end_item) {
+                                      RowsFn rows, BeginFn begin_item, ConsumeFn consume, EndFn end_item,
+                                      FlushFn flush) {
     constexpr int D = Feed<DQ, DP, E>::D;
     constexpr int U = Feed<DQ, DP, E>::U;
     const int G = (c1 > c0) ? (int)((c1 - c0 + 32 * U - 1) / (32 * U)) : 0;
@@ -463,6 +496,7 @@ __device__ __forceinline__ void sweep(Feed<DQ, DP, E>& feed, int items, int64_t 
                     consume(k, xq, xp);
                 }
             }
+            flush();   // one group of chunks done
             if (++slot_c == D) slot_c = 0;
         }
         end_item(it);
@@ -644,9 +678,9 @@ constexpr int kStageBytes = 2048;
 constexpr int kStatsRingBytes = kWarps * kStages * kStageBytes;
 static size_t stats_smem_bytes(int E) { return E == 8 ? (size_t)kStatsRingBytes : 0; }
 
-template <typename T, typename AddFn>
+template <typename T, typename AddFn, typename GroupFn>
 __device__ __forceinline__ void stream_piece_ring(char* ring, const void* row, int64_t c0, int64_t c1, int lane,
-                                                  AddFn add) {
+                                                  AddFn add, GroupFn add_full) {
     constexpr int BT = 8 * (int)sizeof(T);   // bytes per chunk
     constexpr int G = kStageBytes / BT;      // chunks per stage
     constexpr int U = G / 32;                // chunks per lane and stage
@@ -673,6 +707,25 @@ __device__ __forceinline__ void stream_piece_ring(char* ring, const void* row, i
         issue(i + kStages - 1, slot == 0 ? kStages - 1 : slot - 1);
         cp_async_wait<kStages - 1>();
         const char* st = ring + slot * kStageBytes;
+        if (c0 + (i + 1) * G <= c1) {   // a full stage: every lane has all U chunks
+            float x[U][8];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if constexpr (sizeof(T) == 2) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(st + (u * 32 + lane) * 16);
+                    x[u][0] = bf16_lo(v.x); x[u][1] = bf16_hi(v.x); x[u][2] = bf16_lo(v.y); x[u][3] = bf16_hi(v.y);
+                    x[u][4] = bf16_lo(v.z); x[u][5] = bf16_hi(v.z); x[u][6] = bf16_lo(v.w); x[u][7] = bf16_hi(v.w);
+                } else {
+                    const float4 a = *reinterpret_cast<const float4*>(st + (u * 32 + lane) * 16);
+                    const float4 b = *reinterpret_cast<const float4*>(st + G * 16 + (u * 32 + lane) * 16);
+                    x[u][0] = a.x; x[u][1] = a.y; x[u][2] = a.z; x[u][3] = a.w;
+                    x[u][4] = b.x; x[u][5] = b.y; x[u][6] = b.z; x[u][7] = b.w;
+                }
+            }
+            add_full(x, c0 + i * G + lane);
+            slot = (slot + 1 == kStages) ? 0 : slot + 1;
+            continue;
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t k = c0 + i * G + u * 32 + lane;
@@ -698,16 +751,23 @@ __device__ __forceinline__ void stream_piece_ring(char* ring, const void* row, i
 template <typename T, int E>
 __device__ __forceinline__ void stats_piece(char* ring, const void* row, int64_t c0, int64_t c1, bool greedy,
                                             float ah, float al, int lane, Part* dst) {
+    constexpr int UG = kStageBytes / (8 * (int)sizeof(T)) / 32;   // chunks per lane and stage
     if (greedy) {
         LaneMax mx;
         auto f = [&](const float (&x)[E], int64_t e0) { mx.add<E>(x, e0); };
-        if constexpr (E == 8) stream_piece_ring<T>(ring, row, c0, c1, lane, f);
+        // chunk u of the group is chunk k0 + 32 u of the row (this lane's chunks, ascending)
+        auto g = [&](const float (&x)[UG][8], int64_t k0) {
+#pragma unroll
+            for (int u = 0; u < UG; ++u) mx.add<8>(x[u], (k0 + 32 * u) * 8);
+        };
+        if constexpr (E == 8) stream_piece_ring<T>(ring, row, c0, c1, lane, f, g);
         else stream_piece<T, E>(row, c0, c1, lane, f);
         mx.publish(dst, lane);
     } else {
         LaneSum sum;
         auto f = [&](const float (&x)[E], int64_t) { sum.add<E>(x, ah, al); };
-        if constexpr (E == 8) stream_piece_ring<T>(ring, row, c0, c1, lane, f);
+        auto g = [&](const float (&x)[UG][8], int64_t) { sum.add_group<UG>(x, ah, al); };
+        if constexpr (E == 8) stream_piece_ring<T>(ring, row, c0, c1, lane, f, g);
         else stream_piece<T, E>(row, c0, c1, lane, f);
         sum.publish(dst, lane);
     }
@@ -991,6 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
         // ---- one cluster-wide residual sweep over every slot that may be needed
         if (np > 0) {
             Kahan acc;
+            float grp = 0.f;   // this lane's chunk sums of the current group (independent), added once
             float Kq = 0.f, Kp = 0.f, cc = 0.f;
             sweep<DQ, DP, E>(
                 feed, np, c0, c1, lane,
@@ -1007,8 +1068,8 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
                     acc = Kahan();
                 },
                 [&](int64_t, const float (&xq)[E], const float (&xp)[E]) {
-                    if (bonus_sweep) acc.add(target_chunk_sum<E>(xp, Kp, ah, al));
-                    else acc.add(resid_chunk_sum<E>(xq, xp, Kq, Kp, ah, al, cc));
+                    if (bonus_sweep) grp += target_chunk_sum<E>(xp, Kp, ah, al);
+                    else grp += resid_chunk_sum<E>(xq, xp, Kq, Kp, ah, al, cc);
                 },
                 [&](int it) {
                     df tot = acc.value();
@@ -1018,6 +1079,10 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
                         tot = df_add(tot, other);
                     }
                     if (lane == 0) sh.res_part[it][warp] = df_to_f(tot);
+                },
+                [&]() {
+                    acc.add(grp);
+                    grp = 0.f;
                 });
             if (lane == 0 && feed.timeout) sh.to_flag[warp] = 1;
             cluster_sync_all();

@@ -190,6 +190,8 @@ def test_same_seed_same_bytes():
         for _ in range(30):
             g = run_gpu(rule, d, 5, 11, 12)
             for k in ref:
+                if k == "workspace":   # scratch, not an output: unread parts keep old contents
+                    continue
                 assert np.array_equal(ref[k].view(np.uint8), g[k].view(np.uint8)), k
 
 
