@@ -776,6 +776,8 @@ __device__ __forceinline__ void stats_piece(char* ring, const void* row, int64_t
 template <typename DQ, typename DP, int E>
 __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const VerifyParams p) {
     extern __shared__ __align__(16) char stats_smem[];
+    // the verify kernel may be scheduled now: it waits for this grid before reading its results
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     char* ring = stats_smem + (threadIdx.x >> 5) * (kStages * kStageBytes);
     const int L = valid_prefix(p);
@@ -905,6 +907,8 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     const float ah = sh.a_hi, al = sh.a_lo;
     const int nrows = 2 * N + 1;   // part index: draft row i -> i, target row i -> N + i
 
+    // everything above read only the call's inputs; the partials need the stats kernel done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (sh.status == SPEC_ST_OK) {
         // ---- row statistics from the stats kernel's per-segment partials (same order in
         // every CTA, so every CTA holds bit-identical values)
@@ -1387,8 +1391,13 @@ static cudaError_t run_verify(VerifyParams& p, cudaStream_t s, int* info) {
     stats_kernel<DQ, DP, E><<<grid, kThreads, stats_smem_bytes(E), s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = make_config<DQ, DP, E>(p.B * C, C, s, attr);
+    // programmatic dependent launch: the verify kernel's CTAs start their input-only prologue
+    // while the stats kernel drains, and wait (griddepcontrol.wait) before reading its partials
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, verify_kernel<DQ, DP, E>, p);
 }
 
