@@ -748,8 +748,126 @@ __device__ __forceinline__ void stream_piece_ring(char* ring, const void* row, i
     }
 }
 
+// The stats kernel's per-warp ring: kStages stages of kStageBytes in shared memory, each
+// filled by one TMA bulk copy (issued by lane 0) that completes on the stage's mbarrier; every
+// lane waits with a bounded poll.  One instruction per stage moves the data, so the scan's
+// issue slots go to the arithmetic.  Slots and phases persist from piece to piece.
+struct StatsRing {
+    char* base;
+    uint64_t* bar;
+    int lane;
+    unsigned phase;     // parity of the next completion of each slot
+    unsigned pending;   // slots with a copy issued and not yet waited for
+    bool timeout;
+    __device__ __forceinline__ void init(char* b, uint64_t* bars, int ln) {
+        base = b;
+        bar = bars;
+        lane = ln;
+        phase = 0;
+        pending = 0;
+        timeout = false;
+        if (lane == 0) {
+            for (int i = 0; i < kStages; ++i) mbar_init(&bar[i], 1);
+            mbar_init_fence();
+        }
+        __syncwarp();
+    }
+    __device__ __forceinline__ void issue(int slot, const char* src, unsigned bytes) {
+        if (timeout) return;   // after a failed wait nothing new is put in flight
+        pending |= 1u << slot;
+        __syncwarp();          // every lane is done with this slot's previous contents
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_expect_tx(&bar[slot], bytes);
+            bulk_g2s(base + slot * kStageBytes, src, bytes, &bar[slot]);
+        }
+    }
+    __device__ __forceinline__ void wait(int slot) {
+        if (timeout) return;
+        const unsigned parity = (phase >> slot) & 1u;
+        int n = 0;
+        while (!mbar_try_wait(&bar[slot], parity)) {
+            if (++n > kSpinLimit) {
+                timeout = true;   // the slot stays pending; drain() waits for it once more
+                return;
+            }
+        }
+        phase ^= 1u << slot;
+        pending &= ~(1u << slot);
+    }
+    __device__ __forceinline__ void drain() {
+        for (int slot = 0; slot < kStages; ++slot) {
+            if (!((pending >> slot) & 1u)) continue;
+            const unsigned parity = (phase >> slot) & 1u;
+            for (int n = 0; n < kSpinLimit && !mbar_try_wait(&bar[slot], parity); ++n) {
+            }
+        }
+    }
+};
+
+// One piece [c0, c1) of a 16-byte aligned row through the bulk ring: full stages go to
+// add_full (U chunks per lane), the ragged last stage chunk by chunk to add.
+template <typename T, typename AddFn, typename GroupFn>
+__device__ __forceinline__ void stream_piece_bulk(StatsRing& R, const void* row, int64_t c0, int64_t c1, int lane,
+                                                  AddFn add, GroupFn add_full) {
+    constexpr int BT = 8 * (int)sizeof(T);   // bytes per chunk
+    constexpr int G = kStageBytes / BT;      // chunks per stage
+    constexpr int U = G / 32;                // chunks per lane and stage
+    const char* g = reinterpret_cast<const char*>(row) + c0 * BT;
+    const int64_t n = c1 - c0;
+    const int nb = (int)((n + G - 1) / G);
+    auto issue = [&](int i) {
+        if (i < nb) R.issue(i % kStages, g + (int64_t)i * G * BT, (unsigned)(min((int64_t)G, n - (int64_t)i * G) * BT));
+    };
+#pragma unroll
+    for (int i = 0; i < kStages - 1; ++i) issue(i);
+    for (int i = 0; i < nb; ++i) {
+        issue(i + kStages - 1);
+        const int slot = i % kStages;
+        R.wait(slot);
+        const char* st = R.base + slot * kStageBytes;
+        if ((int64_t)(i + 1) * G <= n) {   // a full stage: every lane has all U chunks
+            float x[U][8];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const char* c = st + (u * 32 + lane) * BT;
+                if constexpr (sizeof(T) == 2) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(c);
+                    x[u][0] = bf16_lo(v.x); x[u][1] = bf16_hi(v.x); x[u][2] = bf16_lo(v.y); x[u][3] = bf16_hi(v.y);
+                    x[u][4] = bf16_lo(v.z); x[u][5] = bf16_hi(v.z); x[u][6] = bf16_lo(v.w); x[u][7] = bf16_hi(v.w);
+                } else {
+                    const float4 a = *reinterpret_cast<const float4*>(c);
+                    const float4 b = *reinterpret_cast<const float4*>(c + 16);
+                    x[u][0] = a.x; x[u][1] = a.y; x[u][2] = a.z; x[u][3] = a.w;
+                    x[u][4] = b.x; x[u][5] = b.y; x[u][6] = b.z; x[u][7] = b.w;
+                }
+            }
+            add_full(x, c0 + (int64_t)i * G + lane);
+        } else {
+            const int cnt = (int)(n - (int64_t)i * G);
+            for (int kk = lane; kk < cnt; kk += 32) {
+                float x[8];
+                const char* c = st + kk * BT;
+                if constexpr (sizeof(T) == 2) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(c);
+                    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+                    x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+                } else {
+                    const float4 a = *reinterpret_cast<const float4*>(c);
+                    const float4 b = *reinterpret_cast<const float4*>(c + 16);
+                    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+                }
+                add(x, (c0 + (int64_t)i * G + kk) * 8);
+            }
+        }
+    }
+}
+
+constexpr int kStatsTimeout = -2;   // idx of a partial whose stats piece lost a bounded wait
+
 template <typename T, int E>
-__device__ __forceinline__ void stats_piece(char* ring, const void* row, int64_t c0, int64_t c1, bool greedy,
+__device__ __forceinline__ void stats_piece(StatsRing& ring, const void* row, int64_t c0, int64_t c1, bool greedy,
                                             float ah, float al, int lane, Part* dst) {
     constexpr int UG = kStageBytes / (8 * (int)sizeof(T)) / 32;   // chunks per lane and stage
     if (greedy) {
@@ -760,16 +878,18 @@ __device__ __forceinline__ void stats_piece(char* ring, const void* row, int64_t
 #pragma unroll
             for (int u = 0; u < UG; ++u) mx.add<8>(x[u], (k0 + 32 * u) * 8);
         };
-        if constexpr (E == 8) stream_piece_ring<T>(ring, row, c0, c1, lane, f, g);
+        if constexpr (E == 8) stream_piece_bulk<T>(ring, row, c0, c1, lane, f, g);
         else stream_piece<T, E>(row, c0, c1, lane, f);
         mx.publish(dst, lane);
+        if (ring.timeout && lane == 0) dst->idx = kStatsTimeout;
     } else {
         LaneSum sum;
         auto f = [&](const float (&x)[E], int64_t) { sum.add<E>(x, ah, al); };
         auto g = [&](const float (&x)[UG][8], int64_t) { sum.add_group<UG>(x, ah, al); };
-        if constexpr (E == 8) stream_piece_ring<T>(ring, row, c0, c1, lane, f, g);
+        if constexpr (E == 8) stream_piece_bulk<T>(ring, row, c0, c1, lane, f, g);
         else stream_piece<T, E>(row, c0, c1, lane, f);
         sum.publish(dst, lane);
+        if (ring.timeout && lane == 0) dst->idx = kStatsTimeout;
     }
 }
 
@@ -778,8 +898,10 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const VerifyParams p
     extern __shared__ __align__(16) char stats_smem[];
     // the verify kernel may be scheduled now: it waits for this grid before reading its results
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ __align__(8) uint64_t stats_bars[kWarps][kStages];
     const int lane = threadIdx.x & 31;
-    char* ring = stats_smem + (threadIdx.x >> 5) * (kStages * kStageBytes);
+    StatsRing ring;
+    ring.init(stats_smem + (threadIdx.x >> 5) * (kStages * kStageBytes), stats_bars[threadIdx.x >> 5], lane);
     const int L = valid_prefix(p);
     if (L == 0) return;
     const int64_t n = p.nchunk;
@@ -834,6 +956,8 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const VerifyParams p
         c = 0;
         ++rho;
     }
+    // no TMA copy of this warp may still be writing its ring when the CTA leaves
+    ring.drain();
 }
 
 // ---------------------------------------------------------------------------------------
@@ -914,6 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
         // every CTA, so every CTA holds bit-identical values)
         const int64_t n = p.nchunk;
         const int64_t lw = stats_share(2 * (int64_t)p.cu[Lv] + Lv, n, p.stats_warps);
+        bool stats_to = false;
         for (int r = (greedy ? N : 0) + warp; r < nrows; r += kWarps) {
             // stats row: target row i at g_b + i, draft row i at g_b + N + 1 + i
             const int64_t rho = 2 * (int64_t)base + b + (r < N ? N + 1 + r : r - N);
@@ -927,6 +1052,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
                     e[k] = p.part[rho * kPiecesMax + pk];
                 else
                     e[k] = Part{greedy ? -kInf : kNoRef, 0.f, 0.f, INT_MAX};
+                stats_to |= (e[k].idx == kStatsTimeout);   // that piece's bounded wait gave up
             }
             if (greedy) {
                 const float Kr = warp_max_nan(fmax_nan(e[0].K, e[1].K));
@@ -986,8 +1112,10 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
         }
         bad_row = __syncthreads_or(bad_row);
         zero_q = __syncthreads_or(zero_q);
+        stats_to = __syncthreads_or(stats_to);
         if (tid == 0) {
-            if (bad_row) sh.status = SPEC_ST_BAD_ROW;
+            if (stats_to) sh.status = SPEC_ST_TIMEOUT;
+            else if (bad_row) sh.status = SPEC_ST_BAD_ROW;
             else if (zero_q) sh.status = SPEC_ST_ZERO_DRAFT_PROB;
         }
         __syncthreads();
