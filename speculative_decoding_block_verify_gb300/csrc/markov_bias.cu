@@ -10,9 +10,11 @@
 // At the draft-side shapes (a handful of rows per W2 pass) this is a gather-GEMV: W2 (rank x V)
 // is streamed from HBM once per row group and every loaded W2 element feeds every row of the
 // group from registers, so the bound is W2's bytes, not the FMAs; tensor cores would only
-// add operand staging here.  Layout: a CTA owns a 32 x E column tile; its 8 warps split the
-// rank dimension, each lane keeps (rows x E) float32 accumulators, and the warps' partial sums
-// are added in shared memory in the epilogue.
+// add operand staging here.  Layout: a CTA owns a 32 x E column tile; its 4 warps split the
+// rank dimension (a warp streams rank / 4 rows of the tile, eight 16-byte loads in flight per
+// lane), each lane keeps (rows x E) float32 accumulators, and the warps' partial sums are added
+// in shared memory in the epilogue.  Small CTAs let four of them share an SM, so the ~500
+// column tiles of a 129,280-token vocabulary run as one wave with ~64 KB of W2 in flight per SM.
 
 #include <cfloat>
 
@@ -21,7 +23,7 @@
 
 namespace sv {
 
-constexpr int kBiasThreads = 256;
+constexpr int kBiasThreads = 128;
 constexpr int kBiasWarps = kBiasThreads / 32;
 constexpr int kRowGroup = 8;
 constexpr int kMaxRank = 1024;
@@ -37,10 +39,12 @@ struct BiasParams {
 };
 
 template <typename DT, typename WT, int E>
-__global__ void __launch_bounds__(kBiasThreads) markov_bias_kernel(const BiasParams p) {
+__global__ void __launch_bounds__(kBiasThreads, 4) markov_bias_kernel(const BiasParams p) {
     extern __shared__ float smem[];
     constexpr int kTile = 32 * E;
-    constexpr int UJ = (E == 1) ? 8 : 4;
+    // W2 rows per load group; two groups per lane alternate (one in flight while the other is
+    // multiplied), 64 bytes of registers per group
+    constexpr int UJ = (E == 1) ? 8 : (sizeof(WT) == 2 ? 4 : 2);
     float* w1s = smem;                          // [kRowGroup][R]
     float* red = smem + kRowGroup * p.R;        // [kBiasWarps][kRowGroup][kTile]
     __shared__ int row_ok[kRowGroup];
@@ -50,23 +54,22 @@ __global__ void __launch_bounds__(kBiasThreads) markov_bias_kernel(const BiasPar
     const int r0 = blockIdx.y * kRowGroup;
     const int nr = min(kRowGroup, p.rows - r0);
 
-    // gather the group's W1 rows (float32) - an invalid prev zeroes its row and marks it
-    for (int t = tid; t < kRowGroup * p.R; t += kBiasThreads) {
-        const int r = t / p.R, j = t % p.R;
-        float v = 0.f;
-        if (r < nr) {
-            const int pv = p.prev[r0 + r];
-            if (pv >= 0 && pv < p.V) v = load_elem<WT>(p.W1, (int64_t)pv * p.R + j);
-        }
-        w1s[t] = v;
-    }
+    // gather the group's W1 rows (float32) - an invalid prev zeroes its row and marks it.  The
+    // prev tokens first, then the gather unrolled so that its loads are in flight together.
+    __shared__ int s_prev[kRowGroup];
     if (tid < kRowGroup) {
-        int ok = 0;
-        if (tid < nr) {
-            const int pv = p.prev[r0 + tid];
-            ok = (pv >= 0 && pv < p.V);
-        }
+        int pv = -1;
+        if (tid < nr) pv = p.prev[r0 + tid];
+        const int ok = (pv >= 0 && pv < p.V);
+        s_prev[tid] = ok ? pv : -1;
         row_ok[tid] = ok;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int t = tid; t < kRowGroup * p.R; t += kBiasThreads) {
+        const int r = t / p.R, j = t - r * p.R;
+        const int pv = s_prev[r];
+        w1s[t] = (pv >= 0) ? load_elem<WT>(p.W1, (int64_t)pv * p.R + j) : 0.f;
     }
     __syncthreads();
 
@@ -80,11 +83,13 @@ __global__ void __launch_bounds__(kBiasThreads) markov_bias_kernel(const BiasPar
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
 
-    for (int j = j0; j < j1; j += UJ) {
-        Chunk<WT, E> c[UJ];
+    Chunk<WT, E> ca[UJ], cb[UJ];
+    auto load = [&](Chunk<WT, E>(&c)[UJ], int j) {
 #pragma unroll
         for (int u = 0; u < UJ; ++u)
             if (active && j + u < j1) c[u].load(row_ptr<WT>(p.W2, j + u, V), chunk);
+    };
+    auto fma_group = [&](const Chunk<WT, E>(&c)[UJ], int j) {
 #pragma unroll
         for (int u = 0; u < UJ; ++u) {
             if (active && j + u < j1) {
@@ -100,6 +105,14 @@ __global__ void __launch_bounds__(kBiasThreads) markov_bias_kernel(const BiasPar
                 }
             }
         }
+    };
+    if (j0 < j1) load(ca, j0);
+    for (int j = j0; j < j1; j += 2 * UJ) {
+        if (j + UJ < j1) load(cb, j + UJ);
+        fma_group(ca, j);
+        if (j + UJ >= j1) break;
+        if (j + 2 * UJ < j1) load(ca, j + 2 * UJ);
+        fma_group(cb, j + UJ);
     }
 #pragma unroll
     for (int r = 0; r < kRowGroup; ++r)
@@ -107,17 +120,28 @@ __global__ void __launch_bounds__(kBiasThreads) markov_bias_kernel(const BiasPar
         for (int e = 0; e < E; ++e) red[(warp * kRowGroup + r) * kTile + lane * E + e] = acc[r][e];
     __syncthreads();
 
+    // epilogue: this thread's outputs o = tid + k * threads; the draft logits are loaded first,
+    // all together, then the warps' partial sums are added
     const float qnan = __int_as_float(0x7fffffff);
-    for (int o = tid; o < kRowGroup * kTile; o += kBiasThreads) {
+    constexpr int KO = kRowGroup * kTile / kBiasThreads;
+    float d[KO];
+#pragma unroll
+    for (int k = 0; k < KO; ++k) {
+        const int o = tid + k * kBiasThreads;
+        const int r = o / kTile, ci = o % kTile;
+        const int64_t v = col0 + ci;
+        d[k] = (r < nr && v < V) ? load_elem<DT>(p.draft, (int64_t)(r0 + r) * V + v) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < KO; ++k) {
+        const int o = tid + k * kBiasThreads;
         const int r = o / kTile, ci = o % kTile;
         const int64_t v = col0 + ci;
         if (r < nr && v < V) {
-            float s = 0.f;
+            float sum = 0.f;
 #pragma unroll
-            for (int w = 0; w < kBiasWarps; ++w) s += red[(w * kRowGroup + r) * kTile + ci];
-            const int64_t idx = (int64_t)(r0 + r) * V + v;
-            const float d = load_elem<DT>(p.draft, idx);
-            p.out[idx] = row_ok[r] ? d + s : qnan;
+            for (int w = 0; w < kBiasWarps; ++w) sum += red[(w * kRowGroup + r) * kTile + ci];
+            p.out[(int64_t)(r0 + r) * V + v] = row_ok[r] ? d[k] + sum : qnan;
         }
     }
 }
