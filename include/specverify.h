@@ -20,7 +20,8 @@
  *     stream) and never synchronises the host.  Outputs are valid once the stream reaches
  *     the end of the call's work.  Calls on the same stream are ordered.
  *   - Logit and weight dtypes are SPEC_DTYPE_F32 (float) or SPEC_DTYPE_BF16 (bfloat16).
- *     Arithmetic is float32 per element with float64 per-stream scalars.
+ *     Arithmetic is float32 per element; per-stream scalars are double-float (two float32s,
+ *     about 48 significant bits).
  *   - Return value: SPEC_OK, or a negative SPEC_ERR_* for an error the host can see from the
  *     arguments alone (nothing is launched then), or SPEC_ERR_CUDA when a launch failed.
  *     spec_last_error() gives a one-line description of the last error in this host thread.

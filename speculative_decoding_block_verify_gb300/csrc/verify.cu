@@ -4,30 +4,32 @@
 // §4 "Verification: the guarantee" - "Token by token" (Leviathan et al. 2023), "Block
 // verification" (Sun et al. 2024) with Figure 3, and "Greedy is a different code path".
 //
-// Design (one launch per call):
-//   * one thread-block cluster of C CTAs per stream; CTA c owns a contiguous vocabulary slice
-//     of every row of its stream, split into one contiguous segment per warp (C x 8 segments
-//     per row, in vocabulary order);
-//   * stats sweep: every logit of the stream is read from HBM exactly once, 16-byte cp.async
-//     copies into a per-warp shared-memory ring; each lane keeps, per row, s = sum 2^(l a - K)
-//     against an integer reference K (a = log2(e)/T carried as a_hi + a_lo, so every exponent
-//     is two FMAs with one rounding and the temperature is exact to ~1e-14).  The fast path
-//     has no branch per element; a chunk that would overflow the running sum (or holds a NaN)
-//     takes an exact slow path that raises K;
-//   * one cluster barrier, then every CTA reduces all partials through distributed shared
-//     memory in the same order, so every CTA holds bit-identical row statistics and takes the
-//     same per-stream decisions without further communication; the per-stream scalars (rho,
-//     the running product w, h) are double-float on the float32 pipes;
+// Design (two launches per call, on the caller's stream):
+//   * stats_kernel - every logit of the batch is read from HBM once.  The chunks of all rows,
+//     end to end, are cut into equal contiguous shares, one per warp of a persistent grid.
+//     Each warp streams its share through a ring of shared-memory stages filled by TMA bulk
+//     copies (one elected lane, one mbarrier per stage, bounded waits).  Each lane keeps, per
+//     row piece, s = sum 2^(l a - K) against an integer reference K (a = log2(e)/T carried as
+//     a_hi + a_lo, so every exponent is two FMAs with one rounding and the temperature is exact
+//     to ~1e-14).  A full stage is taken at once: its maximum raises K at most once, then its
+//     terms are independent and enter a Kahan sum once; NaN and +inf poison the row.  Greedy
+//     rows keep the maximum and its lowest index instead.  One partial per (row, piece).
+//   * verify_kernel - one thread-block cluster of C CTAs per stream, launched with
+//     programmatic dependent launch: its prologue (offsets, temperature, tokens, the logits
+//     at the tokens) overlaps the stats kernel's tail, and it waits for that grid before it
+//     reads the partials.  Every CTA reduces the stream's partials in the same order, so all
+//     hold bit-identical row statistics and take the same decisions without communicating;
+//     the per-stream scalars (rho, the running product w, h) are double-float on the float32
+//     pipes.  CTA c owns a contiguous vocabulary slice of every row, one segment per warp.
 //   * block verification: h_N = w_N needs no residual; slot i < N is a candidate only if
 //     eta_i <= w_i (since h_i <= w_i); the residual masses of all candidates and of slot 0 are
-//     computed in one cluster-wide sweep (re-read, mostly from L2), then tau = the largest
-//     candidate with eta_i <= h_i, else 0.  The token-wise rule needs one residual (at tau);
-//   * the draw: a 64-bit fixed-point CDF over the segments (exact integer prefix sums), then
-//     the warp whose segment holds U*R rescans it in the same fixed point and writes the
-//     token.  CTAs arrive at the final cluster barrier as soon as their last distributed-
-//     shared-memory read is done, so none waits for the rescan.
-// Slot 0 is the last pair read by the stats sweep so that its residual (the common tau = 0
-// case at low acceptance) finds it in L2.
+//     computed in one cluster-wide sweep (a second read, partly from L2), then tau = the
+//     largest candidate with eta_i <= h_i, else 0.  The token-wise rule needs one residual (at
+//     tau); when every draft is accepted the sweep sums the bonus row p_N instead;
+//   * the draw: a 64-bit fixed-point CDF over the segments (exact integer prefix sums through
+//     distributed shared memory), then the warp whose segment holds U*R rescans it in the same
+//     fixed point and writes the token.  CTAs arrive at the final cluster barrier as soon as
+//     their last distributed-shared-memory read is done, so none waits for the rescan.
 
 #include <cooperative_groups.h>
 
