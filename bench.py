@@ -244,7 +244,8 @@ def traffic_from_profiles(kernel_tag):
     for line in open(path):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
+            tok = v.split()
+            vals[k.strip()] = tok[0].strip("`") if tok else ""   # the value is the first token
     if vals.get("source_sha256") != sha:
         return None
     try:
