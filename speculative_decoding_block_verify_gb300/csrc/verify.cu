@@ -507,17 +507,38 @@ __device__ __forceinline__ void sweep(Feed<DQ, DP, E>& feed, int items, int64_t 
 
 // Inverse-CDF rescan of one warp segment in 64-bit fixed point (weights times `scale`): the
 // first element whose running sum exceeds t, or - if rounding keeps the segment's sum at or
-// below t - the segment's last positive element.
+// below t - the segment's last positive element.  The segment is taken in groups of U chunks
+// per lane (chunk base + 32 u + lane); the next group's loads are in flight while the current
+// one is scanned, and the U cross-lane scans of a group are independent, so they overlap.
 template <typename DQ, typename DP, int E, bool BONUS>
-__device__ __forceinline__ int rescan_segment(const void* rq, const void* rp, int64_t c0, int64_t c1,
-                                              float Kq, float Kp, float ah, float al, float c, float scale,
-                                              unsigned long long t, int lane) {
-    constexpr int U = 4;
-    unsigned long long run = 0;
-    int y = -1, ylast = -1;
-    for (int64_t base = c0; base < c1 && y < 0; base += 32 * U) {
-        Chunk<DQ, E> cq[U];
-        Chunk<DP, E> cp[U];
+__device__ __forceinline__ void rescan_weights(const Chunk<DQ, E>& cq, const Chunk<DP, E>& cp, float Kq, float Kp,
+                                               float ah, float al, float c, float scale,
+                                               unsigned long long (&qv)[E]) {
+    float xp[E], w[E];
+    cp.unpack(xp);
+    if (BONUS) {
+#pragma unroll
+        for (int j = 0; j < E; ++j) w[j] = ex2(fmaf(xp[j], al, fmaf(xp[j], ah, -Kp)));
+    } else {
+        float xq[E];
+        cq.unpack(xq);
+        resid_weights<E>(xq, xp, Kq, Kp, ah, al, c, w);
+    }
+#pragma unroll
+    for (int j = 0; j < E; ++j) qv[j] = __float2ull_rn(w[j] * scale);
+}
+
+template <typename DQ, typename DP, int E, bool BONUS>
+__device__ __noinline__ int rescan_segment(const void* rq, const void* rp, int64_t c0, int64_t c1, float Kq,
+                                           float Kp, float ah, float al, float c, float scale, unsigned long long t,
+                                           int lane) {
+    // chunks per lane and group: bf16 rows 4, wider rows fewer (two groups stay in registers)
+    constexpr int CB = E * (int)((BONUS ? 0 : sizeof(DQ)) + sizeof(DP));   // bytes per chunk (pair)
+    constexpr int U = (E == 1) ? 4 : (CB <= 32 ? 2 : 1);
+    constexpr int G = 32 * U;
+    Chunk<DQ, E> qa[U], qb[U];
+    Chunk<DP, E> pa[U], pb[U];
+    auto load = [&](Chunk<DQ, E>(&cq)[U], Chunk<DP, E>(&cp)[U], int64_t base) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t k = base + u * 32 + lane;
@@ -526,59 +547,85 @@ __device__ __forceinline__ int rescan_segment(const void* rq, const void* rp, in
                 cp[u].load(rp, k);
             }
         }
+    };
+    unsigned long long run = 0;
+    int ylast = -1;
+    // one group: true once the token is found (y set)
+    auto scan = [&](const Chunk<DQ, E>(&cq)[U], const Chunk<DP, E>(&cp)[U], int64_t base, int& y) -> bool {
+        unsigned long long lsum[U], incl[U];
+        int lpos[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t k = base + u * 32 + lane;
-            unsigned long long qv[E];
-            unsigned long long lsum = 0;
-            int lpos = -1;
+            lsum[u] = 0;
+            lpos[u] = -1;
             if (k < c1) {
-                float xp[E], w[E];
-                cp[u].unpack(xp);
-                if (BONUS) {
-#pragma unroll
-                    for (int j = 0; j < E; ++j) w[j] = ex2(fmaf(xp[j], al, fmaf(xp[j], ah, -Kp)));
-                } else {
-                    float xq[E];
-                    cq[u].unpack(xq);
-                    resid_weights<E>(xq, xp, Kq, Kp, ah, al, c, w);
-                }
+                unsigned long long qv[E];
+                rescan_weights<DQ, DP, E, BONUS>(cq[u], cp[u], Kq, Kp, ah, al, c, scale, qv);
 #pragma unroll
                 for (int j = 0; j < E; ++j) {
-                    qv[j] = __float2ull_rn(w[j] * scale);
-                    lsum += qv[j];
-                    if (qv[j] > 0) lpos = (int)(k * E + j);
+                    lsum[u] += qv[j];
+                    if (qv[j] > 0) lpos[u] = (int)(k * E + j);
                 }
-            } else {
-#pragma unroll
-                for (int j = 0; j < E; ++j) qv[j] = 0;
             }
-            unsigned long long incl = lsum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += n;
-            }
-            const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
-            const unsigned hit = __ballot_sync(0xffffffffu, lsum > 0 && run + incl > t);
-            const int lp_max = __reduce_max_sync(0xffffffffu, lpos);
-            if (lp_max >= 0) ylast = lp_max;
-            if (hit && y < 0) {
-                const int L = __ffs(hit) - 1;
-                int yl = -1;
-                if (lane == L) {
-                    unsigned long long acc = run + incl - lsum;
-#pragma unroll
-                    for (int j = 0; j < E; ++j) {
-                        acc += qv[j];
-                        if (yl < 0 && qv[j] > 0 && acc > t) yl = (int)(k * E + j);
-                    }
-                    if (yl < 0) yl = lpos;
-                }
-                y = __shfl_sync(0xffffffffu, yl, L);
-            }
-            run += total;
+            incl[u] = lsum[u];
         }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {   // U independent inclusive scans, interleaved
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const unsigned long long n = __shfl_up_sync(0xffffffffu, incl[u], o);
+                if (lane >= o) incl[u] += n;
+            }
+        }
+        int uh = -1, L = 0;
+        unsigned long long before = 0;   // fixed-point mass before chunk slice uh
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const unsigned long long total = __shfl_sync(0xffffffffu, incl[u], 31);
+            const unsigned hit = __ballot_sync(0xffffffffu, lsum[u] > 0 && run + incl[u] > t);
+            const int lp_max = __reduce_max_sync(0xffffffffu, lpos[u]);
+            if (uh < 0) {
+                if (lp_max >= 0) ylast = lp_max;
+                if (hit) {
+                    uh = u;
+                    L = __ffs(hit) - 1;
+                    before = run;
+                } else {
+                    run += total;
+                }
+            }
+        }
+        if (uh < 0) return false;
+        // lane L walks its chunk of slice uh
+        int yl = -1;
+        if (lane == L) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (u != uh) continue;
+                const int64_t k = base + u * 32 + lane;
+                unsigned long long qv[E];
+                rescan_weights<DQ, DP, E, BONUS>(cq[u], cp[u], Kq, Kp, ah, al, c, scale, qv);
+                unsigned long long acc = before + incl[u] - lsum[u];
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    acc += qv[j];
+                    if (yl < 0 && qv[j] > 0 && acc > t) yl = (int)(k * E + j);
+                }
+                if (yl < 0) yl = lpos[u];
+            }
+        }
+        y = __shfl_sync(0xffffffffu, yl, L);
+        return true;
+    };
+    int y = -1;
+    load(qa, pa, c0);
+    for (int64_t base = c0; base < c1; base += 2 * G) {
+        if (base + G < c1) load(qb, pb, base + G);
+        if (scan(qa, pa, base, y)) break;
+        if (base + G >= c1) break;
+        if (base + 2 * G < c1) load(qa, pa, base + 2 * G);
+        if (scan(qb, pb, base + G, y)) break;
     }
     return y >= 0 ? y : ylast;
 }
