@@ -106,6 +106,8 @@ struct Shared {
     int to_flag[kWarps];            // a bounded wait of this warp gave up
     int N, status, greedy, tau, sample_seg, sample_bonus;
     unsigned long long sample_t;   // in-segment target (fixed point)
+    unsigned long long sub_sum[kWarps];   // the drawn segment split over the owning CTA's warps
+    int sub_last[kWarps];
     float sample_scale;            // fixed-point scale of the draw's weights
     float a_hi, a_lo;
 };
@@ -505,11 +507,7 @@ __device__ __forceinline__ void sweep(Feed<DQ, DP, E>& feed, int items, int64_t 
     }
 }
 
-// Inverse-CDF rescan of one warp segment in 64-bit fixed point (weights times `scale`): the
-// first element whose running sum exceeds t, or - if rounding keeps the segment's sum at or
-// below t - the segment's last positive element.  The segment is taken in groups of U chunks
-// per lane (chunk base + 32 u + lane); the next group's loads are in flight while the current
-// one is scanned, and the U cross-lane scans of a group are independent, so they overlap.
+// Fixed-point weight (times `scale`) of each element of one chunk pair.
 template <typename DQ, typename DP, int E, bool BONUS>
 __device__ __forceinline__ void rescan_weights(const Chunk<DQ, E>& cq, const Chunk<DP, E>& cp, float Kq, float Kp,
                                                float ah, float al, float c, float scale,
@@ -528,6 +526,11 @@ __device__ __forceinline__ void rescan_weights(const Chunk<DQ, E>& cq, const Chu
     for (int j = 0; j < E; ++j) qv[j] = __float2ull_rn(w[j] * scale);
 }
 
+// Inverse-CDF rescan of one warp segment in 64-bit fixed point (weights times `scale`): the
+// first element whose running sum exceeds t, or - if rounding keeps the segment's sum at or
+// below t - the segment's last positive element.  The segment is taken in groups of U chunks
+// per lane (chunk base + 32 u + lane); the next group's loads are in flight while the current
+// one is scanned, and the U cross-lane scans of a group are independent, so they overlap.
 template <typename DQ, typename DP, int E, bool BONUS>
 __device__ __noinline__ int rescan_segment(const void* rq, const void* rp, int64_t c0, int64_t c1, float Kq,
                                            float Kp, float ah, float al, float c, float scale, unsigned long long t,
@@ -628,6 +631,46 @@ __device__ __noinline__ int rescan_segment(const void* rq, const void* rp, int64
         if (scan(qb, pb, base + G, y)) break;
     }
     return y >= 0 ? y : ylast;
+}
+
+// Fixed-point sum (weights times `scale`) of the chunks [k0, k1) and their last positive
+// element, over the warp (every lane returns both).
+template <typename DQ, typename DP, int E, bool BONUS>
+__device__ __noinline__ void segment_fixed_sum(const void* rq, const void* rp, int64_t k0, int64_t k1, float Kq,
+                                               float Kp, float ah, float al, float c, float scale, int lane,
+                                               unsigned long long& sum, int& last) {
+    constexpr int U = 2;
+    unsigned long long ls = 0;
+    int lp = -1;
+    for (int64_t base = k0; base < k1; base += 32 * U) {
+        Chunk<DQ, E> cq[U];
+        Chunk<DP, E> cp[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = base + u * 32 + lane;
+            if (k < k1) {
+                if (!BONUS) cq[u].load(rq, k);
+                cp[u].load(rp, k);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = base + u * 32 + lane;
+            if (k < k1) {
+                unsigned long long qv[E];
+                rescan_weights<DQ, DP, E, BONUS>(cq[u], cp[u], Kq, Kp, ah, al, c, scale, qv);
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    ls += qv[j];
+                    if (qv[j] > 0) lp = (int)(k * E + j);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    sum = ls;
+    last = __reduce_max_sync(0xffffffffu, lp);
 }
 
 // exponent l a - K as a df (a = ah + al), l finite
@@ -1370,18 +1413,49 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     // every distributed-shared-memory read of this CTA is done: arrive now, wait at the end
     cluster_arrive();
 
-    const bool owner = (sh.sample_seg == crank * kWarps + warp);
-    if (sh.status == SPEC_ST_OK && !greedy && sh.sample_seg >= 0 && owner) {
+    // ---- the rescan of the drawn segment, split over the warps of the CTA that owns it: each
+    // warp sums an eighth in fixed point, the eighth that crosses the target is rescanned
+    if (sh.status == SPEC_ST_OK && !greedy && sh.sample_seg >= 0 && crank == sh.sample_seg / kWarps) {
         const int tau = sh.tau;
-        int y;
-        if (sh.sample_bonus) {
-            y = rescan_segment<DQ, DP, E, true>(nullptr, prow(N), c0, c1, 0.f, sh.rowK[2 * N], ah, al, 0.f,
-                                                sh.sample_scale, sh.sample_t, lane);
-        } else {
-            y = rescan_segment<DQ, DP, E, false>(qrow(tau), prow(tau), c0, c1, sh.rowK[tau], sh.rowK[N + tau], ah,
-                                                 al, sh.cval[tau], sh.sample_scale, sh.sample_t, lane);
+        const bool bonus = sh.sample_bonus != 0;
+        const void* rq = bonus ? nullptr : qrow(tau);
+        const void* rp = bonus ? prow(N) : prow(tau);
+        const float Kq = bonus ? 0.f : sh.rowK[tau], Kp = bonus ? sh.rowK[2 * N] : sh.rowK[N + tau];
+        const float cc = bonus ? 0.f : sh.cval[tau];
+        const int64_t s0 = min(p.nchunk, (int64_t)sh.sample_seg * p.seg_chunks);
+        const int64_t s1 = min(p.nchunk, s0 + p.seg_chunks);
+        const int64_t msub = (s1 - s0 + kWarps - 1) / kWarps;
+        const int64_t w0 = min(s1, s0 + warp * msub), w1 = min(s1, w0 + msub);
+        unsigned long long sub;
+        int last;
+        if (bonus)
+            segment_fixed_sum<DQ, DP, E, true>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, lane, sub, last);
+        else
+            segment_fixed_sum<DQ, DP, E, false>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, lane, sub, last);
+        if (lane == 0) {
+            sh.sub_sum[warp] = sub;
+            sh.sub_last[warp] = last;
         }
-        if (lane == 0) p.out_tok[(int64_t)b * (p.kmax + 1) + tau] = y;
+        __syncthreads();
+        const unsigned long long t = sh.sample_t;
+        unsigned long long before = 0;
+        int wsel = -1, lastpos = -1;
+        for (int w = 0; w < kWarps; ++w) {
+            lastpos = max(lastpos, sh.sub_last[w]);
+            if (wsel < 0) {
+                if (sh.sub_sum[w] > 0 && before + sh.sub_sum[w] > t) wsel = w;
+                else before += sh.sub_sum[w];
+            }
+        }
+        int y = -1;
+        if (wsel < 0) {
+            y = lastpos;   // rounding kept the segment's sum at or below the target
+        } else if (warp == wsel) {
+            y = bonus ? rescan_segment<DQ, DP, E, true>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, t - before, lane)
+                      : rescan_segment<DQ, DP, E, false>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, t - before,
+                                                         lane);
+        }
+        if ((wsel < 0 && tid == 0) || (warp == wsel && lane == 0)) p.out_tok[(int64_t)b * (p.kmax + 1) + tau] = y;
     }
 
     // ---- outputs (CTA rank 0)
