@@ -68,7 +68,7 @@ extern "C" {
 #define SPEC_ST_ZERO_DRAFT_PROB 4 /* T > 0 and q_i(x_i) = 0 (the draft logit at x_i is -inf) */
 #define SPEC_ST_BAD_OFFSETS 5     /* cu_drafts[0] != 0, or the count of stream b or of an
                                      earlier stream is negative or above kmax */
-#define SPEC_ST_TIMEOUT 6         /* reserved: a bounded device wait gave up */
+#define SPEC_ST_TIMEOUT 6         /* a bounded device wait gave up, or the workspace was not zero-filled */
 #define SPEC_ST_NUMERIC 7         /* the distribution to draw from has zero or non-finite mass */
 
 /* limits */
@@ -120,7 +120,8 @@ int dspark_markov_bias(const void* draft_logits, int32_t draft_dtype, int32_t ro
  * n_emitted [B] int32 = tau + 1 (0 when status != 0); status [B] int32 (SPEC_ST_*).
  * diag is optional (NULL = not written): float [cu[B] + B, SPEC_DIAG_COLS], NaN where a
  * value was not computed.
- * workspace: device scratch of at least spec_verify_workspace_bytes(B, kmax) bytes; calls that
+ * workspace: device scratch of at least spec_verify_workspace_bytes(B, kmax) bytes, zero-filled
+ * once before its first use (each call leaves it in a valid state for the next); calls that
  * share a workspace must be ordered (same stream).
  * Rows read: T > 0 reads all 2 N_b + 1 rows of the stream; T = 0 reads the N_b + 1 target
  * rows only.  Status precedence: BAD_OFFSETS, BAD_TEMPERATURE, BAD_TOKEN, BAD_ROW,
@@ -152,9 +153,13 @@ typedef struct {
 
 /*
  * spec_verify_workspace_bytes - device workspace a verify call over B streams with up to
- * kmax drafts each needs (16-byte aligned, caller-allocated, contents need no initialisation;
- * 0 for invalid arguments).  The workspace holds the per-segment row statistics that the
- * stats pass hands to the per-stream pass; it may be reused by later calls on the same stream.
+ * kmax drafts each needs (16-byte aligned, caller-allocated; 0 for invalid arguments).  The
+ * workspace holds, per row, the per-segment statistics that the stats pass hands to the
+ * per-stream pass and a counter of the segments published so far, which lets each stream
+ * start as soon as its own rows are done.  Zero-fill it once before the first call; every
+ * call returns the counters it used to zero, so the workspace may then be reused by later
+ * calls on the same stream, for any B and kmax that fit.  After a call that reported
+ * SPEC_ST_TIMEOUT, zero-fill it again.
  */
 size_t spec_verify_workspace_bytes(int32_t B, int32_t kmax);
 
@@ -185,13 +190,13 @@ int spec_verify_block(const spec_verify_args* args, void* stream);
 
 /*
  * spec_verify_block_static - spec_verify_block without a caller workspace: the stats partials
- * go to a fixed device array of 8 MiB that the library reserves when it is loaded, so the
+ * go to a fixed device array of 8192 x 1040 bytes that the library reserves when it is loaded, so the
  * call allocates no memory at all (for callers that cannot allocate device memory where they
  * verify).  It is an engineering variant of the block verification above; the pages that
  * define the method have no counterpart to it.
  * args->workspace and args->workspace_bytes are ignored.  Capacity: B (2 kmax + 1) <= 8192
  * rows (e.g. B = 256 at kmax = 15); a larger batch returns SPEC_ERR_WORKSPACE and launches
- * nothing.  The array needs no initial contents.  Every call on a device shares it: calls that
+ * nothing.  The array starts zero-filled like every device variable.  Every call on a device shares it: calls that
  * can overlap in time (different streams or host threads) race on it, so the caller must
  * order them.  The first call on each device looks the array's address up
  * (cudaGetSymbolAddress); make that first call outside any stream capture.

@@ -196,7 +196,8 @@ def _verify(fn, cu_drafts, draft_logits, target_logits, draft_tokens, temperatur
         need = spec_verify_workspace_bytes(B, kmax)
         ws = out.get("workspace")
         if ws is None or ws.numel() < need:
-            ws = out["workspace"] = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            # zero-filled once: every call leaves the row counters it used at zero
+            ws = out["workspace"] = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
     a = VerifyArgs()
     a.B, a.V, a.kmax = B, V, kmax
     a.cu_drafts = cu_drafts.data_ptr()

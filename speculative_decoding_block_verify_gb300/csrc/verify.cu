@@ -69,7 +69,7 @@ struct VerifyParams {
     float* diag;
     int64_t nchunk;      // chunks of 8 (or 1) elements per row
     int64_t seg_chunks;  // chunks per warp segment of the cluster kernel's residual sweep
-    struct Part* part;   // workspace: per-row partials of the stats kernel, [rows][kPiecesMax]
+    char* ws;            // workspace: one block of kRowBytes per stats row (see row_block)
     int64_t stats_warps; // warps of the stats kernel's grid
 };
 
@@ -81,10 +81,19 @@ struct Part {
     int idx;
 };
 
-// bytes of workspace a verify call needs: kPiecesMax partials per row; a stream has at most
-// 2 kmax + 1 rows
-static size_t workspace_bytes(int32_t B, int32_t kmax) {
-    return (size_t)B * (size_t)(2 * kmax + 1) * kPiecesMax * sizeof(Part);
+// Workspace: stats row rho owns bytes [rho kRowBytes, (rho + 1) kRowBytes): a 32-bit counter
+// of published partials (in a 16-byte slot), then its kPiecesMax partials.  A row's block sits
+// at the same place for every batch size, and each call leaves the counters of the rows it
+// used at zero, so a zero-filled workspace stays valid from call to call.  A stream has at
+// most 2 kmax + 1 rows.
+constexpr size_t kRowBytes = 16 + kPiecesMax * sizeof(Part);
+static size_t workspace_rows(int32_t B, int32_t kmax) { return (size_t)B * (size_t)(2 * kmax + 1); }
+static size_t workspace_bytes(int32_t B, int32_t kmax) { return workspace_rows(B, kmax) * kRowBytes; }
+__device__ __forceinline__ unsigned* row_counter(const VerifyParams& p, int64_t rho) {
+    return reinterpret_cast<unsigned*>(p.ws + rho * (int64_t)kRowBytes);
+}
+__device__ __forceinline__ Part* row_parts(const VerifyParams& p, int64_t rho) {
+    return reinterpret_cast<Part*>(p.ws + rho * (int64_t)kRowBytes + 16);
 }
 
 struct Shared {
@@ -131,6 +140,36 @@ __device__ __forceinline__ void cluster_sync_all() {
 // poll); the plain path (E = 1) loads directly.
 // ---------------------------------------------------------------------------------------
 constexpr int kSpinLimit = 1 << 20;   // mbarrier polls before a wait gives up (status TIMEOUT)
+
+// Row counters: a stats warp publishes a partial, then adds 1 to its row's counter with
+// release semantics; a verify CTA reads the partials of a row once the counter (read with
+// acquire semantics) equals the row's piece count.  The wait gives up after kRowWaitNs of
+// device time (or a value above the count, which only a non-zero workspace can hold).
+constexpr unsigned long long kRowWaitNs = 4000000000ull;
+
+__device__ __forceinline__ void count_release(unsigned* c) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c) : "memory");
+}
+__device__ __forceinline__ unsigned load_acquire(const unsigned* c) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ bool wait_count(const unsigned* c, unsigned want) {
+    const unsigned long long t0 = global_ns();
+    for (int it = 0; it < (1 << 26); ++it) {
+        const unsigned v = load_acquire(c);
+        if (v == want) return true;
+        if (v > want || global_ns() - t0 > kRowWaitNs) return false;
+        __nanosleep(64);
+    }
+    return false;
+}
 
 template <typename DQ, typename DP, int E>
 struct Feed;
@@ -988,7 +1027,7 @@ __device__ __forceinline__ void stats_piece(StatsRing& ring, const void* row, in
 template <typename DQ, typename DP, int E>
 __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const VerifyParams p) {
     extern __shared__ __align__(16) char stats_smem[];
-    // the verify kernel may be scheduled now: it waits for this grid before reading its results
+    // the verify kernel may be scheduled now: it reads a row's partials once its counter is full
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ __align__(8) uint64_t stats_bars[kWarps][kStages];
     const int lane = threadIdx.x & 31;
@@ -1036,13 +1075,14 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const VerifyParams p
                 ah = a.hi;
                 al = a.lo;
             }
-            Part* dst = p.part + rho * kPiecesMax + (gw - rho * n / lw);
+            Part* dst = row_parts(p, rho) + (gw - rho * n / lw);
             if (draft)
                 stats_piece<DQ, E>(ring, row_ptr<DQ>(p.dq, (int64_t)p.cu[b] + (j - Nb - 1), V), c, c_end, false,
                                    ah, al, lane, dst);
             else
                 stats_piece<DP, E>(ring, row_ptr<DP>(p.dp, (int64_t)p.cu[b] + b + j, V), c, c_end, greedy, ah, al,
                                    lane, dst);
+            if (lane == 0) count_release(row_counter(p, rho));   // lane 0 wrote the partial
         }
         f += c_end - c;
         c = 0;
@@ -1123,60 +1163,104 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     const float ah = sh.a_hi, al = sh.a_lo;
     const int nrows = 2 * N + 1;   // part index: draft row i -> i, target row i -> N + i
 
-    // everything above read only the call's inputs; the partials need the stats kernel done
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (sh.status == SPEC_ST_OK) {
-        // ---- row statistics from the stats kernel's per-segment partials (same order in
-        // every CTA, so every CTA holds bit-identical values)
-        const int64_t n = p.nchunk;
-        const int64_t lw = stats_share(2 * (int64_t)p.cu[Lv] + Lv, n, p.stats_warps);
-        bool stats_to = false;
-        for (int r = (greedy ? N : 0) + warp; r < nrows; r += kWarps) {
-            // stats row: target row i at g_b + i, draft row i at g_b + N + 1 + i
-            const int64_t rho = 2 * (int64_t)base + b + (r < N ? N + 1 + r : r - N);
-            const int64_t first = rho * n / lw;
-            const int cnt = (int)((rho * n + n - 1) / lw - first) + 1;   // pieces of this row
-            Part e[2];
+    // Everything above read only the call's inputs.  The stats kernel writes every row of a
+    // stream with valid offsets and temperature (target rows only when greedy); each row is
+    // waited for here - also when the stream already failed, so that its counters can be reset
+    // at the end - and its partials are read once the row's counter is full.
+    // the per-slot uniforms depend on (seed, step, stream, slot) only
+    if (sh.status == SPEC_ST_OK && !greedy && tid <= N) {
+        const uint4 c = make_uint4((uint32_t)tid, (uint32_t)b, (uint32_t)p.step, (uint32_t)(p.step >> 32));
+        const uint4 wds = philox4x32_10(c, make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
+        sh.u_acc[tid] = uniform24_df(wds.x);
+        sh.u_smp[tid] = wds.y;
+        sh.h[tid] = df{__int_as_float(0x7fffffff), 0.f};
+        sh.r[tid] = df{__int_as_float(0x7fffffff), 0.f};
+    }
+    const bool rows_written = offsets_ok && temp_ok;
+    const int64_t nck = p.nchunk;
+    const int64_t lw = stats_share(2 * (int64_t)p.cu[Lv] + Lv, nck, p.stats_warps);
+    // stats row of part r: target row i at g_b + i, draft row i at g_b + N + 1 + i
+    auto stats_row = [&](int r) { return 2 * (int64_t)base + b + (r < N ? N + 1 + r : r - N); };
+    bool stats_to = false;
+    if (rows_written) {
+        // one row per half-warp (16 rows per pass): lane l of a half holds pieces l, l + 16, ...
+        const bool ok = sh.status == SPEC_ST_OK;
+        const int hl = lane & 15;
+        for (int r0 = (greedy ? N : 0) + 2 * warp; r0 < nrows; r0 += 2 * kWarps) {
+            const int r = r0 + (lane >> 4);
+            const bool have = r < nrows;
+            int cnt = 0;
+            bool full = false;
+            int64_t rho = 0;
+            if (have) {
+                rho = stats_row(r);
+                const int64_t first = rho * nck / lw;
+                cnt = (int)((rho * nck + nck - 1) / lw - first) + 1;   // pieces of this row
+                full = wait_count(row_counter(p, rho), (unsigned)cnt);
+                stats_to |= !full;
+            }
+            if (!ok) continue;
+            // row statistics from the per-piece partials (same order in every CTA, so every
+            // CTA holds bit-identical values)
+            constexpr int kSlots = kPiecesMax / 16;
+            Part e[kSlots];
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int pk = lane + 32 * k;
-                if (pk < cnt)
-                    e[k] = p.part[rho * kPiecesMax + pk];
-                else
+            for (int k = 0; k < kSlots; ++k) {
+                const int pk = hl + 16 * k;
+                if (have && full && pk < cnt) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(row_parts(p, rho) + pk));
+                    e[k] = Part{v.x, v.y, v.z, __float_as_int(v.w)};
+                } else {
                     e[k] = Part{greedy ? -kInf : kNoRef, 0.f, 0.f, INT_MAX};
+                }
                 stats_to |= (e[k].idx == kStatsTimeout);   // that piece's bounded wait gave up
             }
             if (greedy) {
-                const float Kr = warp_max_nan(fmax_nan(e[0].K, e[1].K));
-                const int arg = warp_min_i(min(e[0].K == Kr ? e[0].idx : INT_MAX, e[1].K == Kr ? e[1].idx : INT_MAX));
-                if (lane == 0) {
+                float Kr = e[0].K;
+#pragma unroll
+                for (int k = 1; k < kSlots; ++k) Kr = fmax_nan(Kr, e[k].K);
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) Kr = fmax_nan(Kr, __shfl_xor_sync(0xffffffffu, Kr, o));
+                int arg = INT_MAX;
+#pragma unroll
+                for (int k = 0; k < kSlots; ++k) arg = min(arg, e[k].K == Kr ? e[k].idx : INT_MAX);
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) arg = min(arg, __shfl_xor_sync(0xffffffffu, arg, o));
+                if (have && hl == 0) {
                     sh.rowK[r] = Kr;
                     sh.rowArg[r] = arg;
                     sh.rowZ[r] = df{0.f, 0.f};
                 }
                 continue;
             }
-            const float Kr = warp_max(fmaxf(e[0].K, e[1].K));
+            float Kr = e[0].K;
+#pragma unroll
+            for (int k = 1; k < kSlots; ++k) Kr = fmaxf(Kr, e[k].K);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) Kr = fmaxf(Kr, __shfl_xor_sync(0xffffffffu, Kr, o));
             df z{0.f, 0.f};
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
+            for (int k = 0; k < kSlots; ++k) {
                 const float sc = (e[k].K == Kr) ? 1.f : pow2_int(e[k].K - Kr);
                 z = df_add(z, df_scale(df{e[k].s_hi, e[k].s_lo}, sc));
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
+            for (int o = 8; o > 0; o >>= 1) {
                 const df other{__shfl_xor_sync(0xffffffffu, z.hi, o), __shfl_xor_sync(0xffffffffu, z.lo, o)};
                 z = df_add(z, other);
             }
-            if (lane == 0) {
+            if (have && hl == 0) {
                 sh.rowK[r] = Kr;
                 sh.rowZ[r] = z;
                 sh.rowArg[r] = INT_MAX;
             }
         }
-        __syncthreads();
-
-        // ---- validity of the rows read, q_i(x_i) > 0, per-slot ratios and uniforms
+    }
+    stats_to = __syncthreads_or(stats_to);
+    if (tid == 0 && stats_to && sh.status == SPEC_ST_OK) sh.status = SPEC_ST_TIMEOUT;
+    __syncthreads();
+    if (sh.status == SPEC_ST_OK) {
+        // ---- validity of the rows read, q_i(x_i) > 0, per-slot ratios
         bool bad_row = false, zero_q = false;
         for (int r = (greedy ? N : 0) + tid; r < nrows; r += kThreads) {
             const float K = sh.rowK[r];
@@ -1194,20 +1278,10 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
             }
             sh.rho[tid] = rho;
         }
-        if (!greedy && tid <= N) {
-            const uint4 c = make_uint4((uint32_t)tid, (uint32_t)b, (uint32_t)p.step, (uint32_t)(p.step >> 32));
-            const uint4 wds = philox4x32_10(c, make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
-            sh.u_acc[tid] = uniform24_df(wds.x);
-            sh.u_smp[tid] = wds.y;
-            sh.h[tid] = df{__int_as_float(0x7fffffff), 0.f};
-            sh.r[tid] = df{__int_as_float(0x7fffffff), 0.f};
-        }
         bad_row = __syncthreads_or(bad_row);
         zero_q = __syncthreads_or(zero_q);
-        stats_to = __syncthreads_or(stats_to);
         if (tid == 0) {
-            if (stats_to) sh.status = SPEC_ST_TIMEOUT;
-            else if (bad_row) sh.status = SPEC_ST_BAD_ROW;
+            if (bad_row) sh.status = SPEC_ST_BAD_ROW;
             else if (zero_q) sh.status = SPEC_ST_ZERO_DRAFT_PROB;
         }
         __syncthreads();
@@ -1512,6 +1586,12 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     feed.drain();
     // no CTA may leave while another can still read its shared memory
     cluster_wait();
+    // every CTA of the cluster has read its partials: the row counters go back to zero for the
+    // next call on this workspace
+    if (crank == 0 && rows_written)
+        for (int r = (greedy ? N : 0) + tid; r < nrows; r += kThreads) *row_counter(p, stats_row(r)) = 0u;
+    // the grid completes only after the stats grid (streams with no rows never waited for it)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Uniforms exposed for checking: out[(s * n_slots + i) * 2 + {0, 1}] (exact in double)
@@ -1644,12 +1724,15 @@ static cudaError_t run_verify(VerifyParams& p, cudaStream_t s, int* info) {
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = make_config<DQ, DP, E>(p.B * C, C, s, attr);
-    // programmatic dependent launch: the verify kernel's CTAs start their input-only prologue
-    // while the stats kernel drains, and wait (griddepcontrol.wait) before reading its partials
+    // programmatic dependent launch: the verify kernel's CTAs start while the stats kernel
+    // drains; each stream waits only for its own rows' counters
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, verify_kernel<DQ, DP, E>, p);
+    e = cudaLaunchKernelEx(&cfg, verify_kernel<DQ, DP, E>, p);
+    if (e != cudaSuccess)   // the stats kernel ran: its counts must not reach the next call
+        cudaMemsetAsync(p.ws, 0, workspace_bytes(p.B, p.kmax), s);
+    return e;
 }
 
 template <int E>
@@ -1697,7 +1780,7 @@ static int verify_entry(const spec_verify_args* a, void* stream, int rule, const
     const bool aligned = (a->V % 8 == 0) && ((uintptr_t)a->target_logits % 16 == 0) &&
                          ((uintptr_t)a->draft_logits % 16 == 0);
     p.nchunk = aligned ? a->V / 8 : a->V;
-    p.part = reinterpret_cast<Part*>(a->workspace);
+    p.ws = reinterpret_cast<char*>(a->workspace);
     if (info == nullptr) {
         const size_t need = workspace_bytes(a->B, a->kmax);
         if (a->workspace == nullptr || a->workspace_bytes < need || (uintptr_t)a->workspace % 16 != 0)
@@ -1727,14 +1810,14 @@ extern "C" int spec_verify_block(const spec_verify_args* args, void* stream) {
 // device memory at the point where they verify (an allocator that is not theirs to touch, a
 // memory budget fixed at start-up); for them the stats partials live in one array reserved
 // when the library's module is loaded, so this call allocates nothing.  The array holds
-// kStaticWorkspaceBytes: rows B (2 kmax + 1) of kPiecesMax 16-byte partials each, i.e. up to
-// 8192 rows (for example B = 256 at kmax = 15); larger batches are refused.  Its contents need
-// no initial value (every partial a call reads is written by that call's stats kernel).  All
-// calls share the one array, so calls that may overlap in time (different streams, threads)
-// race on it and must be ordered by the caller.
+// kStaticWorkspaceBytes: B (2 kmax + 1) row blocks (a counter and kPiecesMax 16-byte partials
+// each), i.e. up to 8192 rows (for example B = 256 at kmax = 15); larger batches are refused.
+// Like every device variable it starts zero-filled, which is the state each call leaves its
+// row counters in.  All calls share the one array, so calls that may overlap in time
+// (different streams, threads) race on it and must be ordered by the caller.
 // ---------------------------------------------------------------------------------------
 namespace sv {
-constexpr size_t kStaticWorkspaceBytes = (size_t)8 << 20;
+constexpr size_t kStaticWorkspaceBytes = (size_t)8192 * kRowBytes;
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
 // device address of g_static_workspace on the current device, looked up once per device

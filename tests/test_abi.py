@@ -86,7 +86,8 @@ def test_verify_args_layout_matches_the_header():
 
 def test_workspace_size_and_check(L):
     # one 16-byte partial per (row, stats segment <= 64); a stream has <= 2 kmax + 1 rows
-    assert sv.spec_verify_workspace_bytes(64, 5) == 64 * 11 * 64 * 16
+    # one block per row: a 16-byte counter slot and 64 partials of 16 bytes
+    assert sv.spec_verify_workspace_bytes(64, 5) == 64 * 11 * (16 + 64 * 16)
     assert sv.spec_verify_workspace_bytes(0, 5) == 0
     assert sv.spec_verify_workspace_bytes(-1, 5) == 0
     assert sv.spec_verify_workspace_bytes(4, 33) == 0

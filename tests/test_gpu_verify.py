@@ -241,3 +241,42 @@ def test_uniforms_bit_exact_against_oracle():
         s, i = np.meshgrid(np.arange(n_streams), np.arange(n_slots), indexing="ij")
         ua, us = philox.slot_uniforms_np(seed, np.full(s.shape, step, np.uint64), s, i)
         assert np.array_equal(g[..., 0], ua) and np.array_equal(g[..., 1], us)
+
+
+def _row_counters(ws):
+    """The 32-bit counter at the head of every 1040-byte row block of a workspace."""
+    n = ws.numel() // 1040
+    return ws[: n * 1040].view(n, 1040)[:, :4].contiguous().view(torch.int32).cpu().numpy()
+
+
+@pytest.mark.parametrize("rule", ["tokenwise", "block"])
+def test_workspace_reuse_across_batches(rule):
+    """One zero-filled workspace serves calls of different B, kmax and stream states (a bad
+    token, a greedy stream): the results equal those on fresh workspaces, and after every call
+    each row counter is back at zero."""
+    fn = RULES[rule][1]
+    big = workloads.make_verify_inputs("batch64", 91, B=12, N=5, V=8192)
+    small = workloads.make_verify_inputs("batch64", 92, B=5, N=3, V=8192)
+    d_big = parity.verify_to_device(big, torch)
+    d_small = parity.verify_to_device(small, torch)
+    d_bad = dict(d_big)
+    d_bad["x"] = d_big["x"].clone()
+    d_bad["x"][int(big["cu_drafts"][2])] = 8192          # stream 2: token out of range
+    d_bad["T"] = d_big["T"].clone()
+    d_bad["T"][4] = 0.0                                  # stream 4: greedy
+    cases = [(d_small, 3), (d_big, 5), (d_bad, 5), (d_small, 3), (d_big, 5)]
+    ws = torch.zeros(sv.spec_verify_workspace_bytes(12, 5), dtype=torch.uint8, device="cuda")
+    for d, kmax in cases:
+        B = d["cu"].numel() - 1
+        fresh = parity.to_numpy(fn(d["cu"], d["dq"], d["dp"], d["x"], d["T"], kmax, 7, 1))
+        o = {"accepted_len": torch.empty(B, dtype=torch.int32, device="cuda"),
+             "out_tokens": torch.empty((B, kmax + 1), dtype=torch.int32, device="cuda"),
+             "n_emitted": torch.empty(B, dtype=torch.int32, device="cuda"),
+             "status": torch.empty(B, dtype=torch.int32, device="cuda"),
+             "workspace": ws}
+        got = parity.to_numpy(fn(d["cu"], d["dq"], d["dp"], d["x"], d["T"], kmax, 7, 1, out=o))
+        for k in ("accepted_len", "out_tokens", "n_emitted", "status"):
+            assert np.array_equal(fresh[k], got[k]), k
+        assert not _row_counters(ws).any()
+    st = parity.to_numpy(fn(d_bad["cu"], d_bad["dq"], d_bad["dp"], d_bad["x"], d_bad["T"], 5, 7, 1))["status"]
+    assert st[2] == 2 and st[4] == 0   # SPEC_ST_BAD_TOKEN, and the greedy stream verifies
