@@ -13,12 +13,16 @@
 //     a_hi + a_lo, so every exponent is two FMAs with one rounding and the temperature is exact
 //     to ~1e-14).  A full stage is taken at once: its maximum raises K at most once, then its
 //     terms are independent and enter a Kahan sum once; NaN and +inf poison the row.  Greedy
-//     rows keep the maximum and its lowest index instead.  One partial per (row, piece).
+//     rows keep the maximum and its lowest index instead.  One partial per (row, piece);
+//     after writing it the warp adds 1 to the row's counter in the workspace (release).
 //   * verify_kernel - one thread-block cluster of C CTAs per stream, launched with
 //     programmatic dependent launch: its prologue (offsets, temperature, tokens, the logits
-//     at the tokens) overlaps the stats kernel's tail, and it waits for that grid before it
-//     reads the partials.  Every CTA reduces the stream's partials in the same order, so all
-//     hold bit-identical row statistics and take the same decisions without communicating;
+//     at the tokens, the uniforms) overlaps the stats kernel's tail, and each stream reads a
+//     row's partials as soon as that row's counter (acquire, bounded wait) shows all its
+//     pieces, so streams whose rows are done start while other rows are still being read; the
+//     counters go back to zero when the stream is done.  Every CTA reduces the stream's
+//     partials in the same order, so all hold bit-identical row statistics and take the same
+//     decisions without communicating;
 //     the per-stream scalars (rho, the running product w, h) are double-float on the float32
 //     pipes.  CTA c owns a contiguous vocabulary slice of every row, one segment per warp.
 //   * block verification: h_N = w_N needs no residual; slot i < N is a candidate only if
@@ -27,9 +31,10 @@
 //     largest candidate with eta_i <= h_i, else 0.  The token-wise rule needs one residual (at
 //     tau); when every draft is accepted the sweep sums the bonus row p_N instead;
 //   * the draw: a 64-bit fixed-point CDF over the segments (exact integer prefix sums through
-//     distributed shared memory), then the warp whose segment holds U*R rescans it in the same
-//     fixed point and writes the token.  CTAs arrive at the final cluster barrier as soon as
-//     their last distributed-shared-memory read is done, so none waits for the rescan.
+//     distributed shared memory), then the CTA that owns the segment holding U*R sums its eight
+//     warp slices in the same fixed point, and the warp whose slice crosses the target rescans
+//     it and writes the token.  CTAs arrive at the final cluster barrier as soon as their last
+//     distributed-shared-memory read is done, so the others do not wait for the rescan.
 
 #include <cooperative_groups.h>
 
