@@ -157,9 +157,8 @@ typedef struct {
  * workspace holds, per row, the per-segment statistics that the stats pass hands to the
  * per-stream pass and a counter of the segments published so far, which lets each stream
  * start as soon as its own rows are done.  Zero-fill it once before the first call; every
- * call returns the counters it used to zero, so the workspace may then be reused by later
- * calls on the same stream, for any B and kmax that fit.  After a call that reported
- * SPEC_ST_TIMEOUT, zero-fill it again.
+ * call returns the counters it used to zero (also when a wait gave up), so the workspace may
+ * then be reused by later calls on the same stream, for any B and kmax that fit.
  */
 size_t spec_verify_workspace_bytes(int32_t B, int32_t kmax);
 

@@ -1591,12 +1591,12 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     feed.drain();
     // no CTA may leave while another can still read its shared memory
     cluster_wait();
-    // every CTA of the cluster has read its partials: the row counters go back to zero for the
-    // next call on this workspace
+    // The grid completes only after the stats grid (a stream with no rows, or whose wait gave
+    // up, never waited for it).  Then every stats add has landed and every CTA of the cluster
+    // has read its partials: the row counters go back to zero for the next call.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (crank == 0 && rows_written)
         for (int r = (greedy ? N : 0) + tid; r < nrows; r += kThreads) *row_counter(p, stats_row(r)) = 0u;
-    // the grid completes only after the stats grid (streams with no rows never waited for it)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Uniforms exposed for checking: out[(s * n_slots + i) * 2 + {0, 1}] (exact in double)

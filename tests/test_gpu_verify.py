@@ -280,3 +280,33 @@ def test_workspace_reuse_across_batches(rule):
         assert not _row_counters(ws).any()
     st = parity.to_numpy(fn(d_bad["cu"], d_bad["dq"], d_bad["dp"], d_bad["x"], d_bad["T"], 5, 7, 1))["status"]
     assert st[2] == 2 and st[4] == 0   # SPEC_ST_BAD_TOKEN, and the greedy stream verifies
+
+
+def test_bad_row_counter_times_out_and_heals():
+    """A row counter above its piece count (a workspace that was not zero-filled) makes the
+    stream's bounded wait give up at once with SPEC_ST_TIMEOUT; the other streams are
+    unaffected, the call resets the counter, and the next call on the workspace is exact."""
+    inp = workloads.make_verify_inputs("batch64", 93, B=6, N=4, V=8192)
+    inp["temperature"][:] = np.maximum(inp["temperature"], 0.5)   # every stream samples
+    d = parity.verify_to_device(inp, torch)
+    fresh = parity.to_numpy(sv.spec_verify_block(d["cu"], d["dq"], d["dp"], d["x"], d["T"], 4, 5, 2))
+    assert (fresh["status"] == 0).all()
+    B = 6
+    ws = torch.zeros(sv.spec_verify_workspace_bytes(B, 4), dtype=torch.uint8, device="cuda")
+    cu = inp["cu_drafts"]
+    rho = 2 * int(cu[3]) + 3                              # stream 3's first target row
+    ws[rho * 1040: rho * 1040 + 4].view(torch.int32)[0] = 1 << 20
+    o = {"accepted_len": torch.empty(B, dtype=torch.int32, device="cuda"),
+         "out_tokens": torch.empty((B, 5), dtype=torch.int32, device="cuda"),
+         "n_emitted": torch.empty(B, dtype=torch.int32, device="cuda"),
+         "status": torch.empty(B, dtype=torch.int32, device="cuda"),
+         "workspace": ws}
+    got = parity.to_numpy(sv.spec_verify_block(d["cu"], d["dq"], d["dp"], d["x"], d["T"], 4, 5, 2, out=o))
+    assert got["status"][3] == 6 and got["n_emitted"][3] == 0   # SPEC_ST_TIMEOUT, nothing emitted
+    others = [b for b in range(B) if b != 3]
+    for k in ("accepted_len", "out_tokens", "n_emitted", "status"):
+        assert np.array_equal(fresh[k][others], got[k][others]), k
+    assert not _row_counters(ws).any()
+    again = parity.to_numpy(sv.spec_verify_block(d["cu"], d["dq"], d["dp"], d["x"], d["T"], 4, 5, 2, out=o))
+    for k in ("accepted_len", "out_tokens", "n_emitted", "status"):
+        assert np.array_equal(fresh[k], again[k]), k
