@@ -12,7 +12,9 @@ Legs:
   value     device time of K back-to-back calls (CUDA events on the launching stream), inputs
             resident in HBM;
   e2e       the same calls through the public API with the inputs in pinned host memory: every
-            step copies its inputs host->device and reads the results back;
+            step copies its inputs host->device (into one of two device buffers, on a copy
+            stream, so the next step's copy overlaps this step's kernels) and reads its
+            results (accepted_len, out_tokens, n_emitted, status) back;
   roofline  algorithmic bytes (one read of every logit row) / mean per-launch kernel time,
             against the measured HBM copy bandwidth;
   cpu_baseline / --impl reference   the float64 oracle on the host cores (process pool), on a
@@ -336,17 +338,29 @@ def run_ours(a, dist):
         for k in ("cu_drafts", "draft_logits", "target_logits", "draft_tokens", "temperature"):
             h[k] = s[k].cpu().pin_memory()
         host.append(h)
-    dbuf = {k: torch.empty_like(sets[0][k]) for k in host[0]}
-    hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs[0].items()}
+    # two device input buffers: step i + 1's host-to-device copy (on its own stream) overlaps
+    # step i's kernels; each step still copies all of its inputs and reads back its results
+    dbufs = [{k: torch.empty_like(sets[0][k]) for k in host[0]} for _ in range(2)]
+    copied = [torch.cuda.Event() for _ in range(2)]
+    used = [torch.cuda.Event() for _ in range(2)]
+    copy_stream = torch.cuda.Stream()
+    results = ("accepted_len", "out_tokens", "n_emitted", "status")
+    hout = {k: torch.empty(outs[0][k].shape, dtype=outs[0][k].dtype, pin_memory=True) for k in results}
     h2d = sum(v.numel() * v.element_size() for v in host[0].values())
     d2h = sum(v.numel() * v.element_size() for v in hout.values())
 
     def e2e_step(i):
-        h = host[i % 3]
-        for k in dbuf:
-            dbuf[k].copy_(h[k], non_blocking=True)
+        h, j = host[i % 3], i % 2
+        dbuf = dbufs[j]
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(used[j])   # the kernels that last read this buffer are done
+            for k in dbuf:
+                dbuf[k].copy_(h[k], non_blocking=True)
+            copied[j].record(copy_stream)
+        stream.wait_event(copied[j])
         o = fn(dbuf["cu_drafts"], dbuf["draft_logits"], dbuf["target_logits"], dbuf["draft_tokens"],
                dbuf["temperature"], kmax, 0, i, out=outs[0])
+        used[j].record(stream)
         for k in hout:
             hout[k].copy_(o[k], non_blocking=True)
 
@@ -357,9 +371,10 @@ def run_ours(a, dist):
     dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    copy_stream.wait_stream(stream)   # no copy of the timed steps starts before e0
     for i in range(n_e2e):
         e2e_step(i)
-    e1.record(stream)
+    e1.record(stream)   # after the last step's results: the stream waited for every copy it used
     torch.cuda.synchronize()
     e2e_ms = dist.max(e0.elapsed_time(e1))
     e2e_value = dist.sum(slots_per_step * n_e2e) / (e2e_ms / 1e3)
