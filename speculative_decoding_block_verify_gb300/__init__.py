@@ -168,6 +168,11 @@ def dspark_markov_bias(draft_logits, prev_tokens, W1, W2, out=None, stream=None)
 
 def _verify(fn, cu_drafts, draft_logits, target_logits, draft_tokens, temperature, kmax, seed,
             step, out=None, diag=False, stream=None, workspace=True):
+    """Marshals one verify call.  ``out`` (returned, and reusable by later calls of the same B
+    and kmax on the same stream) holds the four result tensors and the device workspace; a
+    workspace the caller puts in ``out["workspace"]`` must have been zero-filled before its
+    first use (the one allocated here is), since the kernels keep per-row counters there that
+    every call leaves at zero."""
     torch = _torch()
     _dev(cu_drafts, "cu_drafts", torch.int32)
     _dev(target_logits, "target_logits")
