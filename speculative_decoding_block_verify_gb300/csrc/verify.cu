@@ -1262,7 +1262,10 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
         }
     }
     stats_to = __syncthreads_or(stats_to);
-    if (tid == 0 && stats_to && sh.status == SPEC_ST_OK) sh.status = SPEC_ST_TIMEOUT;
+    if (tid == 0 && stats_to) {
+        if (sh.status == SPEC_ST_OK) sh.status = SPEC_ST_TIMEOUT;
+        sh.to_flag[0] = 1;   // the time-bounded waits of the cluster's CTAs may end differently
+    }
     __syncthreads();
     if (sh.status == SPEC_ST_OK) {
         // ---- validity of the rows read, q_i(x_i) > 0, per-slot ratios
@@ -1388,13 +1391,26 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
                     grp = 0.f;
                 });
             if (lane == 0 && feed.timeout) sh.to_flag[warp] = 1;
-            cluster_sync_all();
-            {
-                bool to = false;
-                if (tid < nseg) to = *cluster.map_shared_rank(&sh.to_flag[tid % kWarps], tid / kWarps) != 0;
-                to = __syncthreads_or(to);
-                if (to && tid == 0) sh.status = SPEC_ST_TIMEOUT;
-            }
+        }
+    }
+
+    // ---- every CTA of the cluster meets here exactly once, whatever its status, so the CTAs
+    // cannot part ways at a cluster barrier; a bounded wait that gave up in any of them (their
+    // statuses may differ only there) makes the stream TIMEOUT in all of them
+    cluster_sync_all();
+    {
+        bool to = false;
+        if (tid < nseg) to = *cluster.map_shared_rank(&sh.to_flag[tid % kWarps], tid / kWarps) != 0;
+        to = __syncthreads_or(to);
+        if (to && tid == 0 && sh.status == SPEC_ST_OK) sh.status = SPEC_ST_TIMEOUT;
+        __syncthreads();
+    }
+
+    if (sh.status == SPEC_ST_OK && !greedy) {
+        const bool block = (p.rule == 1);
+        const bool bonus_sweep = sh.sample_bonus != 0;
+        np = sh.n_pass;
+        if (np > 0) {
             // per pass item: r_i = (sum over all segments) / Z_q
             for (int it = warp; it < np && !bonus_sweep; it += kWarps) {
                 df tot{0.f, 0.f};
