@@ -46,9 +46,14 @@ tokens outside [0, V)), BAD_ROW (a read row with NaN / +inf / no finite entry),
 ZERO_DRAFT_PROB (T > 0 and q_i(x_i) = 0 at some slot), NUMERIC (zero residual mass where a
 draw is needed).  A stream with a nonzero status emits nothing.
 
-Near ties: the GPU computes in float32/float64 and this oracle in float64, so a decision
-whose uniform lies within TIE_REL (relative) of its threshold is flagged; such streams are
-counted and excluded from the exact comparison.
+Near ties: the GPU computes in float32 and double-float, this oracle in float64, so a
+decision whose uniform lies within TIE_REL (relative) of its threshold is flagged, and so is a
+draw whose target U R lies within TIE_REL (relative) of a CDF value that decides the token.
+For such a stream the result also lists every outcome a computation with that much relative
+error may reach: each (tau, tokens) pair obtained by flipping any subset of the near
+comparisons (and nothing else), with, for that tau, every positive-weight token whose CDF
+interval meets the draw's window.  A flagged stream is then checked against that list, not
+skipped.
 """
 
 import math
@@ -116,25 +121,50 @@ def block_tau(eta, h):
     return tau
 
 
+def window_bounds(t, total):
+    """The CDF window of a draw with target t = U R: [t (1 - TIE_REL), t (1 + TIE_REL)]."""
+    return t * (1.0 - TIE_REL), t * (1.0 + TIE_REL)
+
+
 def inverse_cdf(weights, u):
-    """(Y, margin): Y = smallest v with C(v) >= u * R; margin = relative distance of u*R to
-    the two thresholds that decide Y, C(Y) and C(Y-1), each relative to the threshold itself
-    (a small margin is a near tie)."""
-    c = np.cumsum(np.asarray(weights, np.float64))
+    """(Y, window): Y = the smallest v with C(v) >= u * R (C the ascending-index cumulative sum
+    of the non-negative weights, R their total).  ``window`` lists, in ascending order, every
+    token with positive weight whose CDF interval [C(v-1), C(v)] meets window_bounds(u R): the
+    tokens a sampler whose partial sums carry a relative error below TIE_REL may return.  Y is
+    always one of them; more than one is a near tie."""
+    w = np.asarray(weights, np.float64)
+    c = np.cumsum(w)
     total = float(c[-1])
     t = u * total
-    y = int(np.searchsorted(c, t, side="left"))
-    y = min(y, len(c) - 1)
-    hi = float(c[y])
-    margin = abs(t - hi) / hi
-    if y > 0 and float(c[y - 1]) > 0.0:
-        lo = float(c[y - 1])
-        margin = min(margin, abs(t - lo) / lo)
-    return y, margin
+    y = min(int(np.searchsorted(c, t, side="left")), len(c) - 1)
+    lo_t, hi_t = window_bounds(t, total)
+    lo = min(int(np.searchsorted(c, lo_t, side="left")), len(c) - 1)
+    hi = min(int(np.searchsorted(c, hi_t, side="left")), len(c) - 1)
+    window = [v for v in range(lo, hi + 1) if w[v] > 0.0]
+    if y not in window:   # only when every weight is zero; the caller rejects that total
+        window = sorted(set(window) | {y})
+    return y, window
 
 
 def _near(a, b):
+    """A comparison a <= b is a near tie when a lies within TIE_REL (relative) of b."""
     return abs(a - b) <= TIE_REL * max(abs(a), abs(b))
+
+
+def _flip_outcomes(passed, near, decide, limit=10):
+    """Every tau reachable by flipping any subset of the near comparisons (at most ``limit`` of
+    them are enumerated), in first-seen order starting with the unflipped tau."""
+    idx = [i for i in range(len(passed)) if near[i]][:limit]
+    seen = []
+    for mask in range(1 << len(idx)):
+        flipped = list(passed)
+        for j, i in enumerate(idx):
+            if (mask >> j) & 1:
+                flipped[i] = not flipped[i]
+        t = decide(flipped)
+        if t not in seen:
+            seen.append(t)
+    return seen
 
 
 # ----------------------------------------------------------------------------------------
@@ -143,7 +173,7 @@ def _near(a, b):
 
 def _empty_result(n, status):
     return {"status": status, "tau": 0, "emitted": [], "n_emitted": 0, "tie": False,
-            "tie_kind": None, "diag": np.full((n + 1, DIAG_COLS), np.nan)}
+            "tie_kind": None, "outcomes": [], "diag": np.full((n + 1, DIAG_COLS), np.nan)}
 
 
 def temperature_ok(T):
@@ -156,7 +186,9 @@ def verify_stream(rule, q_rows, p_rows, x, T, seed, step, stream):
 
     q_rows: N draft logit rows, p_rows: N+1 target logit rows (any float dtype; widened
     exactly to float64), x: N draft tokens, T: temperature (0 = greedy).
-    Returns a dict: status, tau, emitted (list), n_emitted, tie, tie_kind, diag [(N+1), 8].
+    Returns a dict: status, tau, emitted (list), n_emitted, tie, tie_kind, outcomes (a list of
+    (tau, tokens) pairs: every result a computation within the near-tie window may give, the
+    exact one first), diag [(N+1), 8].
     """
     n = len(x)
     V = len(p_rows[0])
@@ -200,37 +232,69 @@ def verify_stream(rule, q_rows, p_rows, x, T, seed, step, stream):
     return _block(res, ps, qs, xs, log_rho, seed, step, stream)
 
 
-def _finish(res, tau, xs, weights, u_sample):
+def _draw_weights_total_ok(weights):
     total = float(np.sum(weights))
-    if not (total > 0.0 and math.isfinite(total)):
+    return total > 0.0 and math.isfinite(total)
+
+
+def _finish(res, taus, xs, weights_at, u_sample_at):
+    """Draw at the decided tau (taus[0]) and at every alternative tau; fill the result."""
+    tau = taus[0]
+    weights = weights_at(tau)
+    if not _draw_weights_total_ok(weights):
         out = _empty_result(len(xs), STATUS_NUMERIC)
         out["diag"] = res["diag"]
         return out
-    y, margin = inverse_cdf(weights, u_sample)
-    if margin <= TIE_REL and not res["tie"]:
+    y, window = inverse_cdf(weights, u_sample_at(tau))
+    if len(window) > 1 and not res["tie"]:
         res["tie"], res["tie_kind"] = True, "sample"
+    outcomes = [(tau, window)]
+    for t in taus[1:]:
+        wt = weights_at(t)
+        if _draw_weights_total_ok(wt):
+            outcomes.append((t, inverse_cdf(wt, u_sample_at(t))[1]))
     res["tau"] = tau
     res["emitted"] = xs[:tau] + [y]
     res["n_emitted"] = tau + 1
+    res["outcomes"] = outcomes
     return res
+
+
+def _tokenwise_tau(passed):
+    """tau of the token-wise rule: the first rejected slot, N if none."""
+    for i, ok in enumerate(passed):
+        if not ok:
+            return i
+    return len(passed)
 
 
 def _tokenwise(res, ps, qs, xs, log_rho, seed, step, stream):
     n = len(xs)
-    for i in range(n):
-        u, us = philox.slot_uniforms(seed, step, stream, i)
-        acc = min(1.0, math.exp(log_rho[i]))
-        if _near(u, acc) and not res["tie"]:
-            res["tie"], res["tie_kind"] = True, "accept"
-        if u <= acc:
-            continue
-        p = np.exp(ps[i])
-        q = np.exp(qs[i])
-        wts = residual_weights(1.0, p, q)
-        res["diag"][i, D_R] = float(np.sum(wts))
-        return _finish(res, i, xs, wts, us)
-    _, us = philox.slot_uniforms(seed, step, stream, n)
-    return _finish(res, n, xs, np.exp(ps[n]), us)
+    uni = [philox.slot_uniforms(seed, step, stream, i) for i in range(n + 1)]
+    acc = [min(1.0, math.exp(log_rho[i])) for i in range(n)]
+    passed = [uni[i][0] <= acc[i] for i in range(n)]
+    near = [_near(uni[i][0], acc[i]) for i in range(n)]
+    tau = _tokenwise_tau(passed)
+    # the comparisons that were evaluated: slots 0..tau (all of them when tau = N)
+    if any(near[i] for i in range(min(tau + 1, n))):
+        res["tie"], res["tie_kind"] = True, "accept"
+    taus = _flip_outcomes(passed, near, _tokenwise_tau)
+
+    def weights_at(t):
+        if t == n:
+            return np.exp(ps[n])
+        return residual_weights(1.0, np.exp(ps[t]), np.exp(qs[t]))
+
+    if tau < n:
+        res["diag"][tau, D_R] = float(np.sum(weights_at(tau)))
+    return _finish(res, taus, xs, weights_at, lambda t: uni[t][1])
+
+
+def block_tie_range(tau, n):
+    """The slots whose comparison eta_i <= h_i decides tau = max{i : eta_i <= h_i}: tau itself
+    and every slot above it (all of 1..N when tau = 0).  A near comparison below tau cannot
+    change tau on its own."""
+    return range(max(tau, 1), n + 1)
 
 
 def _block(res, ps, qs, xs, log_rho, seed, step, stream):
@@ -246,18 +310,31 @@ def _block(res, ps, qs, xs, log_rho, seed, step, stream):
     h = block_h(w, r)
     for i in range(1, n + 1):
         diag[i, D_H] = h[i]
-    eta = [float("nan")] + [philox.slot_uniforms(seed, step, stream, i - 1)[0]
-                            for i in range(1, n + 1)]
+    uni = [philox.slot_uniforms(seed, step, stream, i) for i in range(n + 1)]
+    eta = [float("nan")] + [uni[i - 1][0] for i in range(1, n + 1)]
     tau = block_tau(eta, h)
-    # a comparison whose flip would change tau: every i >= tau (all of them when tau = 0)
-    for i in range(max(tau, 1), n + 1):
+    for i in block_tie_range(tau, n):
         if _near(eta[i], h[i]) and not res["tie"]:
             res["tie"], res["tie_kind"] = True, "block"
-    _, us = philox.slot_uniforms(seed, step, stream, tau)
-    if tau == n:
-        return _finish(res, tau, xs, np.exp(ps[n]), us)
-    wts = residual_weights(w[tau], np.exp(ps[tau]), np.exp(qs[tau]))
-    return _finish(res, tau, xs, wts, us)
+    # passed / near indexed by slot - 1 (slots 1..N)
+    passed = [eta[i] <= h[i] for i in range(1, n + 1)]
+    near = [_near(eta[i], h[i]) for i in range(1, n + 1)]
+
+    def decide(flags):
+        t = 0
+        for j, ok in enumerate(flags):
+            if ok:
+                t = j + 1
+        return t
+
+    taus = _flip_outcomes(passed, near, decide)
+
+    def weights_at(t):
+        if t == n:
+            return np.exp(ps[n])
+        return residual_weights(w[t], np.exp(ps[t]), np.exp(qs[t]))
+
+    return _finish(res, taus, xs, weights_at, lambda t: uni[t][1])
 
 
 def _greedy(p_rows, xs):
@@ -271,9 +348,11 @@ def _greedy(p_rows, xs):
         if argmax_lowest(pr[i]) != xs[i]:
             tau = i
             break
+    y = argmax_lowest(pr[tau])
     res["tau"] = tau
-    res["emitted"] = xs[:tau] + [argmax_lowest(pr[tau])]
+    res["emitted"] = xs[:tau] + [y]
     res["n_emitted"] = tau + 1
+    res["outcomes"] = [(tau, [y])]
     return res
 
 
@@ -290,7 +369,9 @@ def verify_batch(rule, cu_drafts, draft_logits, target_logits, draft_tokens, tem
     draft_tokens [cu[B]], temperature [B].  ``streams`` restricts the work to a subset (the
     other streams' outputs are left at their fill values: status -1).
     Returns dict of numpy arrays: accepted_len, out_tokens [B, kmax+1] (-1 padded),
-    n_emitted, status, diag [cu[B] + B, 8], tie (bool) and tie_kind (list).
+    n_emitted, status, diag [cu[B] + B, 8], tie (bool), tie_kind (list) and outcomes (list of
+    each stream's admissible (tau, tokens) pairs; empty for a stream that was not verified or
+    whose status is not OK).
     """
     cu = [int(v) for v in np.asarray(cu_drafts)]
     B = len(cu) - 1
@@ -304,6 +385,7 @@ def verify_batch(rule, cu_drafts, draft_logits, target_logits, draft_tokens, tem
         "diag": np.full((max(cu[-1] + B, 0), DIAG_COLS), np.nan),
         "tie": np.zeros(B, bool),
         "tie_kind": [None] * B,
+        "outcomes": [[] for _ in range(B)],
     }
     # Streams are packed from row 0 in order.  The first stream whose draft count lies
     # outside [0, kmax] (or cu[0] != 0) leaves the row positions of every later stream
@@ -327,6 +409,7 @@ def verify_batch(rule, cu_drafts, draft_logits, target_logits, draft_tokens, tem
         out["status"][b] = r["status"]
         out["tie"][b] = r["tie"]
         out["tie_kind"][b] = r["tie_kind"]
+        out["outcomes"][b] = r["outcomes"]
         if r["status"] == STATUS_OK:
             out["accepted_len"][b] = r["tau"]
             out["n_emitted"][b] = r["n_emitted"]

@@ -69,10 +69,11 @@ def test_markov_bias_invalid_prev_and_in_place():
 
 
 @pytest.mark.parametrize("rule", [ov.RULE_TOKENWISE, ov.RULE_BLOCK])
-@pytest.mark.parametrize("name,n_steps,stride", [("tiny", 300, 1), ("single_bias", 10000, 50)])
+@pytest.mark.parametrize("name,n_steps,stride", [("tiny", 300, 1), ("single_bias", 10000, 10)])
 def test_bias_then_verify_end_to_end(rule, name, n_steps, stride):
     """Markov bias -> verify on the GPU against float64 bias -> verify in the oracle.  The GPU
-    runs every step; the oracle checks every stride-th step (float64 over V = 129,280 is slow)."""
+    runs every step; the oracle checks every stride-th step (for the single-stream V = 129,280
+    workload: the 1,000-step subset 0, 10, 20, ... of 10,000 steps, on the host cores)."""
     inp = workloads.make_verify_inputs(name, 2000)
     bias = workloads.make_bias_inputs(name, 2000)
     dt = torch.bfloat16 if inp["dtype"] == "bf16" else torch.float32
@@ -81,23 +82,30 @@ def test_bias_then_verify_end_to_end(rule, name, n_steps, stride):
                                    _t(bias["W1"], dt), _t(bias["W2"], dt))
     ref_q = om.markov_bias(inp["draft_logits"], bias["prev"], bias["W1"], bias["W2"])
     fn = sv.spec_verify_block if rule == ov.RULE_BLOCK else sv.spec_verify_tokenwise
-    ties = exact = 0
     taus = []
+    gpu = {}
     for step in range(n_steps):
-        g = fn(d["cu"], biased, d["dp"], d["x"], d["T"], inp["kmax"], 0, step)
-        if step % stride:
-            taus.append(int(g["accepted_len"][0]))
-            continue
-        g = parity.to_numpy(g)
-        taus.append(int(g["accepted_len"][0]))
-        o = ov.verify_batch(rule, inp["cu_drafts"], ref_q, inp["target_logits"],
-                            inp["draft_tokens"], inp["temperature"], inp["kmax"], 0, step)
-        st = parity.compare_verify(g, o, inp["cu_drafts"], [0], inp["draft_tokens"], inp["V"],
-                                   check_diag=False)
-        ties += st["ties"]
-        exact += st["exact"]
-    checked = len(range(0, n_steps, stride))
-    assert exact + ties == checked and ties <= max(2, parity.MAX_TIE_FRACTION * checked)
+        g = fn(d["cu"], biased, d["dp"], d["x"], d["T"], inp["kmax"], 0, step, diag=(step % stride == 0))
+        if step % stride == 0:
+            gpu[step] = parity.to_numpy(g)
+            taus.append(int(gpu[step]["accepted_len"][0]))
+        else:
+            taus.append(g["accepted_len"][0])
+    taus = [int(t) for t in taus]
+    runs = [(rule, 0, st) for st in range(0, n_steps, stride)]
+    host = {"cu": inp["cu_drafts"], "dq": ref_q, "dp": np.asarray(inp["target_logits"], np.float64),
+            "x": inp["draft_tokens"], "T": inp["temperature"]}
+    ref = parity.oracle_runs(host, inp["kmax"], runs, [0], torch, runs_per_task=max(1, len(runs) // 16))
+    totals = {"streams": 0, "ties": 0, "exact": 0, "tie_match": 0}
+    for run in runs:
+        # the biased rows differ from the oracle's float64 ones by the float32 bias rounding, so
+        # the diag columns are compared by test_markov_bias_parity's bound, not here
+        st = parity.compare_verify(gpu[run[2]], ref[run], inp["cu_drafts"], [0], inp["draft_tokens"],
+                                   inp["V"], check_diag=False)
+        for k in totals:
+            totals[k] += st[k]
+    assert totals["exact"] + totals["ties"] == len(runs)
+    parity.check_tie_totals(totals)
     assert len(taus) == n_steps and min(taus) >= 0 and max(taus) <= 5
 
 
@@ -177,9 +185,10 @@ def test_pick_k_batch_small_brute_force():
         assert abs(e - v) <= 1e-6 * v
 
 
-def test_adaptive_then_ragged_verify():
-    """Per-stream pick over B = 128 (H = 7168), then the ragged block verify over V = 129,280
-    with the oracle's k, checked against the oracle on a spread of streams."""
+@pytest.mark.parametrize("rule", [ov.RULE_TOKENWISE, ov.RULE_BLOCK])
+def test_adaptive_then_ragged_verify(rule):
+    """Per-stream pick over B = 128 (H = 7168), then the ragged verify over V = 129,280 with
+    the oracle's k (streams with k = 0 included), every stream checked against the oracle."""
     c, h, w, vm = _pick_inputs(11)
     g = sv.adaptive_pick_k(h, w, c["beta"], vm, mode=0)
     a = oc.prefix_survival(oc.confidence(c["hidden"], c["w"], c["beta"]))
@@ -191,19 +200,16 @@ def test_adaptive_then_ragged_verify():
     inp = workloads.make_verify_inputs("adaptive128", 12, k=k, backend="torch")
     d = {"cu": inp["cu_drafts"], "dq": inp["draft_logits"], "dp": inp["target_logits"],
          "x": inp["draft_tokens"], "T": inp["temperature"]}
-    out = parity.to_numpy(sv.spec_verify_block(d["cu"], d["dq"], d["dp"], d["x"], d["T"], 5, 0, 0,
-                                               diag=True))
-
-    class RowView:
-        def __init__(self, t):
-            self.t = t
-
-        def __getitem__(self, i):
-            return self.t[int(i)].float().cpu().numpy()
-
+    fn = sv.spec_verify_block if rule == ov.RULE_BLOCK else sv.spec_verify_tokenwise
+    runs = [(rule, 0, st) for st in range(2)]
+    gpu = {run: parity.to_numpy(fn(d["cu"], d["dq"], d["dp"], d["x"], d["T"], 5, 0, run[2], diag=True))
+           for run in runs}
+    ref = parity.oracle_runs(d, 5, runs, list(range(128)), torch)
     cu = inp["cu_drafts"].cpu().numpy()
-    streams = list(range(0, 128, 8))
-    o = ov.verify_batch(ov.RULE_BLOCK, cu, RowView(d["dq"]), RowView(d["dp"]),
-                        inp["draft_tokens"].cpu().numpy(), inp["temperature"].cpu().numpy(), 5, 0, 0,
-                        streams=streams)
-    parity.compare_verify(out, o, cu, streams, inp["draft_tokens"].cpu().numpy(), inp["V"])
+    x = inp["draft_tokens"].cpu().numpy()
+    totals = {"streams": 0, "ties": 0, "exact": 0, "tie_match": 0}
+    for run in runs:
+        st = parity.compare_verify(gpu[run], ref[run], cu, range(128), x, inp["V"])
+        for key in totals:
+            totals[key] += st[key]
+    parity.check_tie_totals(totals)

@@ -1,9 +1,10 @@
 """GPU parity of spec_verify_tokenwise / spec_verify_block against the float64 oracle.
 
 Every call goes through the C ABI (ctypes binding).  Accepted lengths, emitted tokens and
-status codes must match exactly outside the near ties the oracle flags (a uniform within
-1e-6 relative of its threshold); diagnostic probabilities, residual masses and log
-normalisers must agree within 1e-5 relative.
+status codes must match exactly; where the oracle flags a near tie (a uniform within 1e-6
+relative of its threshold) the GPU's (tau, token) must be one of the outcomes the oracle
+lists for it.  Diagnostic probabilities, residual masses and log normalisers must agree within
+1e-5 relative on every stream.
 """
 
 import numpy as np
@@ -64,7 +65,7 @@ def check(inp, rule_name, seeds_steps, d=None, streams=None, dq=None, dp=None, c
                                    inp["V"], check_diag=check_diag)
         for k in totals:
             totals[k] += st[k]
-    assert totals["ties"] <= max(2, parity.MAX_TIE_FRACTION * totals["streams"]), totals
+    parity.check_tie_totals(totals)
     return totals
 
 
@@ -205,32 +206,46 @@ def test_empty_batch():
     assert g["status"].size == 0
 
 
-@pytest.mark.parametrize("rule", ["tokenwise", "block"])
-def test_batch64_full_size(rule):
-    """B = 64, k = 5, V = 129,280 bf16, in the launch configuration the bench times."""
-    inp = workloads.make_verify_inputs("batch64", 3000, backend="torch")
-    d = {"cu": inp["cu_drafts"], "dq": inp["draft_logits"], "dp": inp["target_logits"],
-         "x": inp["draft_tokens"], "T": inp["temperature"]}
-    host = dict(inp)
-    host["cu_drafts"] = inp["cu_drafts"].cpu().numpy()
-    host["draft_tokens"] = inp["draft_tokens"].cpu().numpy()
-    host["temperature"] = inp["temperature"].cpu().numpy()
-    check(host, rule, [(0, 0), (0, 1)], d=d, dq=RowView(d["dq"]), dp=RowView(d["dp"]))
+def full_size_parity(name, seeds, rule_names, steps, streams=None, kmax=None):
+    """GPU calls of the given rules over `steps` consecutive steps on each seeded full-size
+    input set, every listed stream checked against the oracle (run on the host cores)."""
+    totals = {"streams": 0, "ties": 0, "exact": 0, "tie_match": 0}
+    for seed in seeds:
+        inp = workloads.make_verify_inputs(name, seed, backend="torch")
+        d = {"cu": inp["cu_drafts"], "dq": inp["draft_logits"], "dp": inp["target_logits"],
+             "x": inp["draft_tokens"], "T": inp["temperature"]}
+        B = inp["B"]
+        k = inp["kmax"] if kmax is None else kmax
+        ss = list(range(B)) if streams is None else streams
+        runs = [(RULES[r][0], 0, st) for r in rule_names for st in range(steps)]
+        gpu = {}
+        for r in rule_names:
+            for st in range(steps):
+                gpu[(RULES[r][0], 0, st)] = run_gpu(r, d, k, 0, st)
+        ref = parity.oracle_runs(d, k, runs, ss, torch, runs_per_task=max(1, len(runs) // 4))
+        cu = inp["cu_drafts"].cpu().numpy()
+        x = inp["draft_tokens"].cpu().numpy()
+        for run in runs:
+            st = parity.compare_verify(gpu[run], ref[run], cu, ss, x, inp["V"])
+            for key in totals:
+                totals[key] += st[key]
+        del d, inp
+        torch.cuda.empty_cache()
+    parity.check_tie_totals(totals)
+    return totals
 
 
-def test_batch256_k9_fp32_full_size_sampled():
-    """B = 256, k = 9, V = 129,280 fp32, block only; the oracle checks a spread of streams."""
-    inp = workloads.make_verify_inputs("batch256_k9", 4000, backend="torch")
-    d = {"cu": inp["cu_drafts"], "dq": inp["draft_logits"], "dp": inp["target_logits"],
-         "x": inp["draft_tokens"], "T": inp["temperature"]}
-    host = dict(inp)
-    host["cu_drafts"] = inp["cu_drafts"].cpu().numpy()
-    host["draft_tokens"] = inp["draft_tokens"].cpu().numpy()
-    host["temperature"] = inp["temperature"].cpu().numpy()
-    streams = list(range(0, 256, 16)) + [255]
-    check(host, "block", [(0, 0)], d=d, streams=streams, dq=RowView(d["dq"]), dp=RowView(d["dp"]))
-    del d, inp
-    torch.cuda.empty_cache()
+def test_batch64_full_size():
+    """B = 64, k = 5, V = 129,280 bf16, in the launch configuration the bench times: 20 steps
+    per rule on each of two input sets, every stream."""
+    t = full_size_parity("batch64", [3000, 3017], ["tokenwise", "block"], 20)
+    assert t["streams"] == 2 * 2 * 20 * 64
+
+
+def test_batch256_k9_fp32_full_size():
+    """B = 256, k = 9, V = 129,280 fp32, block only: every stream for two steps."""
+    t = full_size_parity("batch256_k9", [4000], ["block"], 2)
+    assert t["streams"] == 2 * 256
 
 
 def test_uniforms_bit_exact_against_oracle():
