@@ -100,6 +100,15 @@ def residual_weights(w, p, q):
     return np.maximum(0.0, w * np.asarray(p, np.float64) - np.asarray(q, np.float64))
 
 
+def residual_gross(w, p, q):
+    """sum_v [w p(v) > q(v)] w p(v): the positive part's gross mass, an upper bound of the
+    residual mass.  Float32 per-element arithmetic computes each term of the residual with an
+    error proportional to w p(v) + q(v), so where the residual is a small difference of large
+    terms its attainable relative accuracy is set by this mass, not by the residual itself."""
+    wp = w * np.asarray(p, np.float64)
+    return float(np.sum(np.where(wp > np.asarray(q, np.float64), wp, 0.0)))
+
+
 def block_h(w, r):
     """h_1..h_N (index 0 unused, NaN) from w_0..w_N and r_0..r_{N-1}."""
     n = len(w) - 1
@@ -173,7 +182,8 @@ def _flip_outcomes(passed, near, decide, limit=10):
 
 def _empty_result(n, status):
     return {"status": status, "tau": 0, "emitted": [], "n_emitted": 0, "tie": False,
-            "tie_kind": None, "outcomes": [], "diag": np.full((n + 1, DIAG_COLS), np.nan)}
+            "tie_kind": None, "outcomes": [], "diag": np.full((n + 1, DIAG_COLS), np.nan),
+            "gross": np.full(n + 1, np.nan)}
 
 
 def temperature_ok(T):
@@ -244,6 +254,7 @@ def _finish(res, taus, xs, weights_at, u_sample_at):
     if not _draw_weights_total_ok(weights):
         out = _empty_result(len(xs), STATUS_NUMERIC)
         out["diag"] = res["diag"]
+        out["gross"] = res["gross"]
         return out
     y, window = inverse_cdf(weights, u_sample_at(tau))
     if len(window) > 1 and not res["tie"]:
@@ -287,6 +298,7 @@ def _tokenwise(res, ps, qs, xs, log_rho, seed, step, stream):
 
     if tau < n:
         res["diag"][tau, D_R] = float(np.sum(weights_at(tau)))
+        res["gross"][tau] = residual_gross(1.0, np.exp(ps[tau]), np.exp(qs[tau]))
     return _finish(res, taus, xs, weights_at, lambda t: uni[t][1])
 
 
@@ -307,6 +319,7 @@ def _block(res, ps, qs, xs, log_rho, seed, step, stream):
     for i in range(0, n):
         r[i] = float(np.sum(residual_weights(w[i], np.exp(ps[i]), np.exp(qs[i]))))
         diag[i, D_R] = r[i]
+        res["gross"][i] = residual_gross(w[i], np.exp(ps[i]), np.exp(qs[i]))
     h = block_h(w, r)
     for i in range(1, n + 1):
         diag[i, D_H] = h[i]
@@ -371,7 +384,8 @@ def verify_batch(rule, cu_drafts, draft_logits, target_logits, draft_tokens, tem
     Returns dict of numpy arrays: accepted_len, out_tokens [B, kmax+1] (-1 padded),
     n_emitted, status, diag [cu[B] + B, 8], tie (bool), tie_kind (list) and outcomes (list of
     each stream's admissible (tau, tokens) pairs; empty for a stream that was not verified or
-    whose status is not OK).
+    whose status is not OK), gross [cu[B] + B] (residual_gross of each slot where the residual
+    was computed, NaN elsewhere).
     """
     cu = [int(v) for v in np.asarray(cu_drafts)]
     B = len(cu) - 1
@@ -386,6 +400,7 @@ def verify_batch(rule, cu_drafts, draft_logits, target_logits, draft_tokens, tem
         "tie": np.zeros(B, bool),
         "tie_kind": [None] * B,
         "outcomes": [[] for _ in range(B)],
+        "gross": np.full(max(cu[-1] + B, 0), np.nan),
     }
     # Streams are packed from row 0 in order.  The first stream whose draft count lies
     # outside [0, kmax] (or cu[0] != 0) leaves the row positions of every later stream
@@ -416,4 +431,5 @@ def verify_batch(rule, cu_drafts, draft_logits, target_logits, draft_tokens, tem
             out["out_tokens"][b, :len(r["emitted"])] = r["emitted"]
         if float(temps[b]) > 0.0 and r["status"] in (STATUS_OK, STATUS_NUMERIC):
             out["diag"][cu[b] + b: cu[b] + b + n + 1] = r["diag"]
+            out["gross"][cu[b] + b: cu[b] + b + n + 1] = r["gross"]
     return out

@@ -152,3 +152,15 @@ def test_tokenwise_acceptance_rate_is_one_minus_tv():
         r = verify.verify_stream(0, [q], [p, p], x, 1.0, seed=6, step=step, stream=0)
         acc += r["tau"] == 1
     assert abs(acc / M - want) < 4 * np.sqrt(want * (1 - want) / M)
+
+
+def test_residual_gross_bounds_the_residual():
+    """residual_gross is the positive part's w p mass: >= the residual, equal when q = 0 on
+    that part, and 0 when w p <= q everywhere."""
+    from oracle import verify as v
+    p = np.array([0.5, 0.3, 0.2])
+    q = np.array([0.1, 0.6, 0.3])
+    g = v.residual_gross(1.0, p, q)
+    assert g == 0.5 and float(v.residual_weights(1.0, p, q).sum()) == pytest.approx(0.4)
+    assert v.residual_gross(1.0, p, np.array([0.0, 1.0, 1.0])) == 0.5
+    assert v.residual_gross(0.1, p, q) == 0.0
