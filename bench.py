@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rule", default="block", choices=["block", "tokenwise"])
     ap.add_argument("--no-secondary", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle leg (profiling runs)")
     ap.add_argument("--cpu-sample", type=int, default=512,
                     help="oracle stream-verifies for cpu_baseline (about 10-15 s of CPU work)")
     ap.add_argument("--ref-sample", type=int, default=16,
@@ -276,6 +278,59 @@ def algorithmic_bytes(inp):
     return rows * V * es
 
 
+def run_e2e(a, dist, fn, sets, outs, kmax, slots_per_step, stream):
+    """The same calls through the public API with the inputs in pinned host memory."""
+    import torch
+    host = []
+    for s in sets:
+        h = {}
+        for k in ("cu_drafts", "draft_logits", "target_logits", "draft_tokens", "temperature"):
+            h[k] = s[k].cpu().pin_memory()
+        host.append(h)
+    # two device input buffers: step i + 1's host-to-device copy (on its own stream) overlaps
+    # step i's kernels; each step still copies all of its inputs and reads back its results
+    dbufs = [{k: torch.empty_like(sets[0][k]) for k in host[0]} for _ in range(2)]
+    copied = [torch.cuda.Event() for _ in range(2)]
+    used = [torch.cuda.Event() for _ in range(2)]
+    copy_stream = torch.cuda.Stream()
+    results = ("accepted_len", "out_tokens", "n_emitted", "status")
+    hout = {k: torch.empty(outs[0][k].shape, dtype=outs[0][k].dtype, pin_memory=True) for k in results}
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h = sum(v.numel() * v.element_size() for v in hout.values())
+
+    def e2e_step(i):
+        h, j = host[i % 3], i % 2
+        dbuf = dbufs[j]
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(used[j])   # the kernels that last read this buffer are done
+            for k in dbuf:
+                dbuf[k].copy_(h[k], non_blocking=True)
+            copied[j].record(copy_stream)
+        stream.wait_event(copied[j])
+        o = fn(dbuf["cu_drafts"], dbuf["draft_logits"], dbuf["target_logits"], dbuf["draft_tokens"],
+               dbuf["temperature"], kmax, 0, i, out=outs[0])
+        used[j].record(stream)
+        for k in hout:
+            hout[k].copy_(o[k], non_blocking=True)
+
+    n_e2e = max(3, min(a.steps, 30))
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    copy_stream.wait_stream(stream)   # no copy of the timed steps starts before e0
+    for i in range(n_e2e):
+        e2e_step(i)
+    e1.record(stream)   # after the last step's results: the stream waited for every copy it used
+    torch.cuda.synchronize()
+    e2e_ms = dist.max(e0.elapsed_time(e1))
+    e2e_value = dist.sum(slots_per_step * n_e2e) / (e2e_ms / 1e3)
+
+    return {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
 def run_ours(a, dist):
     import torch
 
@@ -331,54 +386,9 @@ def run_ours(a, dist):
     traffic = traffic_from_profiles(f"verify_{a.rule}_batch64")
     status_ok = all(int((o["status"] != 0).sum()) == 0 for o in outs)
 
-    # e2e through the public API with host buffers
-    host = []
-    for s in sets:
-        h = {}
-        for k in ("cu_drafts", "draft_logits", "target_logits", "draft_tokens", "temperature"):
-            h[k] = s[k].cpu().pin_memory()
-        host.append(h)
-    # two device input buffers: step i + 1's host-to-device copy (on its own stream) overlaps
-    # step i's kernels; each step still copies all of its inputs and reads back its results
-    dbufs = [{k: torch.empty_like(sets[0][k]) for k in host[0]} for _ in range(2)]
-    copied = [torch.cuda.Event() for _ in range(2)]
-    used = [torch.cuda.Event() for _ in range(2)]
-    copy_stream = torch.cuda.Stream()
-    results = ("accepted_len", "out_tokens", "n_emitted", "status")
-    hout = {k: torch.empty(outs[0][k].shape, dtype=outs[0][k].dtype, pin_memory=True) for k in results}
-    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
-    d2h = sum(v.numel() * v.element_size() for v in hout.values())
-
-    def e2e_step(i):
-        h, j = host[i % 3], i % 2
-        dbuf = dbufs[j]
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(used[j])   # the kernels that last read this buffer are done
-            for k in dbuf:
-                dbuf[k].copy_(h[k], non_blocking=True)
-            copied[j].record(copy_stream)
-        stream.wait_event(copied[j])
-        o = fn(dbuf["cu_drafts"], dbuf["draft_logits"], dbuf["target_logits"], dbuf["draft_tokens"],
-               dbuf["temperature"], kmax, 0, i, out=outs[0])
-        used[j].record(stream)
-        for k in hout:
-            hout[k].copy_(o[k], non_blocking=True)
-
-    n_e2e = max(3, min(a.steps, 30))
-    for i in range(3):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    copy_stream.wait_stream(stream)   # no copy of the timed steps starts before e0
-    for i in range(n_e2e):
-        e2e_step(i)
-    e1.record(stream)   # after the last step's results: the stream waited for every copy it used
-    torch.cuda.synchronize()
-    e2e_ms = dist.max(e0.elapsed_time(e1))
-    e2e_value = dist.sum(slots_per_step * n_e2e) / (e2e_ms / 1e3)
-
+    e2e = None
+    if not a.no_e2e:
+        e2e = run_e2e(a, dist, fn, sets, outs, kmax, slots_per_step, stream)
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": elapsed_ms / a.steps, "higher_is_better": True,
@@ -395,7 +405,7 @@ def run_ours(a, dist):
                      "kernel": "one verify call: stats_kernel then verify_kernel on one stream",
                      "algorithmic_bytes_per_launch": alg, "mean_launch_us": mean_launch_ms * 1e3,
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)"},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "clocks": clk,
         "all_status_ok": status_ok,
     }
@@ -546,7 +556,7 @@ def main():
             print(json.dumps(run_reference(a, dist)), flush=True)
             return
         cpu = None
-        if dist.rank == 0:
+        if dist.rank == 0 and not a.no_cpu_baseline:
             cpu = oracle_sample(a.cpu_sample, a.rule)   # before the first GPU call (spawned pool)
         res = run_ours(a, dist)
         if dist.rank == 0:

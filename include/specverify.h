@@ -153,12 +153,13 @@ typedef struct {
 
 /*
  * spec_verify_workspace_bytes - device workspace a verify call over B streams with up to
- * kmax drafts each needs (16-byte aligned, caller-allocated; 0 for invalid arguments).  The
- * workspace holds, per row, the per-segment statistics that the stats pass hands to the
- * per-stream pass and a counter of the segments published so far, which lets each stream
- * start as soon as its own rows are done.  Zero-fill it once before the first call; every
- * call returns the counters it used to zero (also when a wait gave up), so the workspace may
- * then be reused by later calls on the same stream, for any B and kmax that fit.
+ * kmax drafts each needs (16-byte aligned, caller-allocated; 0 for B = 0 and for invalid
+ * arguments): 256 + 1536 B (2 kmax + 1) + 1024 B (kmax + 1) bytes.  It holds the claim tickets
+ * of the two persistent kernels, per row the statistics partials and a counter of the pieces
+ * published, the per-slot and per-stream scalars that one kernel of the call hands to the
+ * next, and the residual sweep's work list.  Zero-fill it once before the first call; every
+ * call returns its tickets and counters to zero (also when a bounded wait gave up), so the
+ * workspace may then be reused by later calls on the same stream, for any B and kmax that fit.
  */
 size_t spec_verify_workspace_bytes(int32_t B, int32_t kmax);
 
@@ -188,17 +189,22 @@ int spec_verify_tokenwise(const spec_verify_args* args, void* stream);
 int spec_verify_block(const spec_verify_args* args, void* stream);
 
 /*
- * spec_verify_block_static - spec_verify_block without a caller workspace: the stats partials
- * go to a fixed device array of 8192 x 1040 bytes that the library reserves when it is loaded, so the
- * call allocates no memory at all (for callers that cannot allocate device memory where they
- * verify).  It is an engineering variant of the block verification above; the pages that
+ * spec_verify_block_static - spec_verify_block without a caller workspace: the workspace is a
+ * fixed device array of 16 MiB (16,777,216 bytes) that the library reserves when it is loaded,
+ * so the call allocates no memory at all.  It is for callers that cannot allocate device memory
+ * where they verify (an allocator that is not theirs to touch, a memory budget fixed at
+ * start-up).  It is an engineering variant of the block verification above; the pages that
  * define the method have no counterpart to it.
- * args->workspace and args->workspace_bytes are ignored.  Capacity: B (2 kmax + 1) <= 8192
- * rows (e.g. B = 256 at kmax = 15); a larger batch returns SPEC_ERR_WORKSPACE and launches
- * nothing.  The array starts zero-filled like every device variable.  Every call on a device shares it: calls that
- * can overlap in time (different streams or host threads) race on it, so the caller must
- * order them.  The first call on each device looks the array's address up
- * (cudaGetSymbolAddress); make that first call outside any stream capture.
+ * args->workspace and args->workspace_bytes are ignored.  Capacity: a batch whose
+ * spec_verify_workspace_bytes(B, kmax) exceeds the array (e.g. B = 512 at kmax = 16) returns
+ * SPEC_ERR_WORKSPACE and launches nothing; B = 256 at kmax = 15 (15.6 MiB) fits.  The argument
+ * checks of spec_verify_block come first, so a bad shape or dtype gets the same code as there.
+ * The array starts zero-filled like every device variable, and every call leaves it so.
+ * Every call on a device shares it: calls that can overlap in time (different streams or host
+ * threads) race on it, so the caller must order them.  The first call on each device looks the
+ * array's address up (cudaGetSymbolAddress) and keeps it for the life of the process: make
+ * that first call outside any stream capture, and do not use this call across a reset of the
+ * device's context (cudaDeviceReset), after which the kept address is no longer valid.
  * Errors: as spec_verify_block, plus SPEC_ERR_WORKSPACE for a batch above the capacity.
  */
 int spec_verify_block_static(const spec_verify_args* args, void* stream);
@@ -206,9 +212,10 @@ int spec_verify_block_static(const spec_verify_args* args, void* stream);
 /*
  * spec_verify_launch_info - the launch configuration a verify call with these arguments
  * would use (no launch, no device data read; only the scalar fields and the two logit
- * pointers' alignment are examined).  cluster_size: CTAs per stream; resident_clusters: how
- * many such clusters the current device holds at once; elems_per_load: 8 when the rows take
- * the 16-byte vector path, 1 otherwise.
+ * pointers' alignment are examined).  cluster_size: CTAs that one stream's decision and draw
+ * use (1: one CTA per stream); resident_clusters: CTAs of the persistent residual-sweep grid
+ * (all resident at once); elems_per_load: 8 when the rows take the 16-byte vector path, 1
+ * otherwise.
  * Errors: as spec_verify_tokenwise (without the NULL checks of the tensor pointers), and
  * SPEC_ERR_ARG when an output pointer is NULL.
  */

@@ -4,60 +4,51 @@
 // §4 "Verification: the guarantee" - "Token by token" (Leviathan et al. 2023), "Block
 // verification" (Sun et al. 2024) with Figure 3, and "Greedy is a different code path".
 //
-// Design (two launches per call, on the caller's stream):
-//   * stats_kernel - every logit of the batch is read from HBM once.  The chunks of all rows,
-//     end to end, are cut into equal contiguous shares, one per warp of a persistent grid.
-//     Each warp streams its share through a ring of shared-memory stages filled by TMA bulk
-//     copies (one elected lane, one mbarrier per stage, bounded waits).  Each lane keeps, per
-//     row piece, s = sum 2^(l a - K) against an integer reference K (a = log2(e)/T carried as
-//     a_hi + a_lo, so every exponent is two FMAs with one rounding and the temperature is exact
-//     to ~1e-14).  A full stage is taken at once: its maximum raises K at most once, then its
-//     terms are independent and enter a Kahan sum once; NaN and +inf poison the row.  Greedy
-//     rows keep the maximum and its lowest index instead.  One partial per (row, piece);
-//     after writing it the warp adds 1 to the row's counter in the workspace (release).
-//   * verify_kernel - one thread-block cluster of C CTAs per stream, launched with
-//     programmatic dependent launch: its prologue (offsets, temperature, tokens, the logits
-//     at the tokens, the uniforms) overlaps the stats kernel's tail, and each stream reads a
-//     row's partials as soon as that row's counter (acquire, bounded wait) shows all its
-//     pieces, so streams whose rows are done start while other rows are still being read; the
-//     counters go back to zero when the stream is done.  Every CTA reduces the stream's
-//     partials in the same order, so all hold bit-identical row statistics and take the same
-//     decisions without communicating;
-//     the per-stream scalars (rho, the running product w, h) are double-float on the float32
-//     pipes.  CTA c owns a contiguous vocabulary slice of every row, one segment per warp.
-//   * block verification: h_N = w_N needs no residual; slot i < N is a candidate only if
-//     eta_i <= w_i (since h_i <= w_i); the residual masses of all candidates and of slot 0 are
-//     computed in one cluster-wide sweep (a second read, partly from L2), then tau = the
-//     largest candidate with eta_i <= h_i, else 0.  The token-wise rule needs one residual (at
-//     tau); when every draft is accepted the sweep sums the bonus row p_N instead;
-//   * the draw: a 64-bit fixed-point CDF over the segments (exact integer prefix sums through
-//     distributed shared memory), then the CTA that owns the segment holding U*R sums its eight
-//     warp slices in the same fixed point, and the warp whose slice crosses the target rescans
-//     it and writes the token.  CTAs arrive at the final cluster barrier as soon as their last
-//     distributed-shared-memory read is done, so the others do not wait for the rescan.
-
-#include <cooperative_groups.h>
+// Design: four launches per call on the caller's stream, chained by programmatic dependent
+// launch (each kernel's prologue overlaps its predecessor's tail; griddepcontrol.wait orders
+// the data).  No kernel waits for another kernel's CTAs, so none can deadlock.
+//   * stats_kernel (persistent): every logit of the batch is read from HBM once.  The chunks of
+//     all rows, end to end, are cut into equal contiguous shares, one per warp, so every warp
+//     streams the same bytes without any claim or hand-off; a share goes through a ring of
+//     shared-memory stages filled by TMA bulk copies and leaves one partial per row it touches:
+//     (integer reference K, sum of 2^(l a - K)) for T > 0, (maximum, lowest index) for T = 0.
+//     a = log2(e) / T is carried as a_hi + a_lo, so each exponent is two FMAs and the
+//     temperature is exact to ~1e-14.
+//   * decide_kernel (one CTA per stream): the row normalisers from the partials, the ratios
+//     rho_i and the clipped running product w_i in double-float, the statuses, and the
+//     decision - greedy tau, token-wise tau, or block verification's candidate slots (eta_i <=
+//     w_i, since h_i <= w_i) plus slot 0; every slot whose residual may be needed becomes a
+//     sweep item, and the items' segments are appended to the sweep's work list.
+//   * sweep_kernel (persistent): the residual masses sum_v max(0, c 2^(lp a - Kp) -
+//     2^(lq a - Kq)), c = w_i Z_q / Z_p, of every item, one sum per segment, with the warps of
+//     the whole GPU claiming runs of segments - a stream with many candidates no longer waits
+//     for a few SMs.  These reads are the only ones beyond the algorithmic bytes.
+//   * finish_kernel (one CTA per stream): r_i, h_i = r_i / (r_i + 1 - w_i), tau, then the draw:
+//     a 64-bit fixed-point CDF over the drawn item's segment sums picks the segment, its eight
+//     slices are summed in the same fixed point by the CTA's warps, and the warp whose slice
+//     crosses the target rescans it.
+// Every bounded wait that gives up turns the stream to SPEC_ST_TIMEOUT; nothing traps.
 
 #include <cfloat>
 #include <climits>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "df.cuh"
 #include "host_util.h"
 
-namespace cg = cooperative_groups;
-
 namespace sv {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxCluster = 8;
 constexpr int kMaxRows = 2 * SPEC_MAX_KMAX + 1;
-constexpr int kRingBytesPerCta = 56 * 1024;
 constexpr float kNoRef = -1e30f;     // reference of a lane that has seen no finite logit
+constexpr int kSegs = 64;            // residual segments per row: the draw's CDF resolution
 constexpr int kPiecesMax = 64;       // stats partials per row
-
-struct Part;
+constexpr int kSegsPerClaim = 2;     // a sweep claim spans 2 segments of one row pair
+constexpr int kStatsThreads = 256;   // threads of a stats CTA
+constexpr int kStatsWarps = kStatsThreads / 32;
 
 struct VerifyParams {
     int32_t B, V, kmax, rule;
@@ -73,229 +64,100 @@ struct VerifyParams {
     int32_t* status;
     float* diag;
     int64_t nchunk;      // chunks of 8 (or 1) elements per row
-    int64_t seg_chunks;  // chunks per warp segment of the cluster kernel's residual sweep
-    char* ws;            // workspace: one block of kRowBytes per stats row (see row_block)
-    int64_t stats_warps; // warps of the stats kernel's grid
+    int64_t seg_chunks;  // chunks per residual segment
+    int32_t nseg;        // segments per row (<= kSegs)
+    int64_t stats_warps; // warps of the stats grid
+    char* ws;            // workspace (layout below)
+    char* list;          // the sweep's work list: the end of the workspace the caller passed
 };
 
-// Per-warp partial of one row.  T > 0: K = integer reference, (s_hi, s_lo) = sum 2^(l a - K).
-// T = 0: K = the segment maximum, idx = its lowest index.
+// Per-piece partial of one row.  T > 0: K = integer reference, (s_hi, s_lo) = sum 2^(l a - K).
+// T = 0: K = the piece maximum, idx = its lowest index.
 struct Part {
     float K;
     float s_hi, s_lo;
     int idx;
 };
 
-// Workspace: stats row rho owns bytes [rho kRowBytes, (rho + 1) kRowBytes): a 32-bit counter
-// of published partials (in a 16-byte slot), then its kPiecesMax partials.  A row's block sits
-// at the same place for every batch size, and each call leaves the counters of the rows it
-// used at zero, so a zero-filled workspace stays valid from call to call.  A stream has at
-// most 2 kmax + 1 rows.
-constexpr size_t kRowBytes = 16 + kPiecesMax * sizeof(Part);
-static size_t workspace_rows(int32_t B, int32_t kmax) { return (size_t)B * (size_t)(2 * kmax + 1); }
-static size_t workspace_bytes(int32_t B, int32_t kmax) { return workspace_rows(B, kmax) * kRowBytes; }
-__device__ __forceinline__ unsigned* row_counter(const VerifyParams& p, int64_t rho) {
-    return reinterpret_cast<unsigned*>(p.ws + rho * (int64_t)kRowBytes);
-}
-__device__ __forceinline__ Part* row_parts(const VerifyParams& p, int64_t rho) {
-    return reinterpret_cast<Part*>(p.ws + rho * (int64_t)kRowBytes + 16);
-}
-
-struct Shared {
-    float res_part[SPEC_MAX_KMAX + 1][kWarps];
-    float rowK[kMaxRows];
-    df rowZ[kMaxRows];
-    int rowArg[kMaxRows];
-    df rho[SPEC_MAX_KMAX];
-    df w[SPEC_MAX_KMAX + 1];
-    df h[SPEC_MAX_KMAX + 1];
-    df r[SPEC_MAX_KMAX + 1];
-    df u_acc[SPEC_MAX_KMAX + 1];
-    uint32_t u_smp[SPEC_MAX_KMAX + 1];
-    float cval[SPEC_MAX_KMAX + 1];     // residual weight scale w_i Z_q / Z_p per slot
-    float lq[SPEC_MAX_KMAX], lp[SPEC_MAX_KMAX];
-    int x[SPEC_MAX_KMAX];
-    int pass_list[SPEC_MAX_KMAX + 1];
-    int n_pass;
-    int to_flag[kWarps];            // a bounded wait of this warp gave up
-    int N, status, greedy, tau, sample_seg, sample_bonus;
-    unsigned long long sample_t;   // in-segment target (fixed point)
-    unsigned long long sub_sum[kWarps];   // the drawn segment split over the owning CTA's warps
-    int sub_last[kWarps];
-    float sample_scale;            // fixed-point scale of the draw's weights
+// ---------------------------------------------------------------------------------------
+// Workspace.  A 256-byte header (the two claim tickets, the valid stream prefix, the number of
+// sweep claims), then one block of kRowBytes per stats row; the sweep's work list sits at the
+// very end of the buffer the caller passed, so that it never lands on the row counters of a
+// call with a larger batch on the same buffer.
+// Stream b owns stats rows g_b = 2 cu[b] + b .. g_b + 2 N_b: its target rows 0..N_b, then its
+// draft rows 0..N_b-1.  A row's block holds its piece counter and partials, its statistics
+// (decide_kernel), and - in target row i's block - slot i's scalars and the segment sums of
+// slot i's sweep item; the stream's own scalars sit in its first row's block.  The state that
+// must be zero between calls (tickets, counters) sits at the same place for every B, and every
+// call returns it to zero, so a zero-filled workspace stays valid from call to call.
+// ---------------------------------------------------------------------------------------
+struct WsHeader {
+    unsigned long long reserved;       // zero
+    unsigned long long ticket_sweep;   // next sweep claim
+    unsigned long long sweep_total;    // sweep claims appended by decide_kernel
+    int32_t L;                         // streams [0, L) have valid offsets
+};
+struct RowStat {
+    float K;          // reference exponent (T > 0) or maximum (T = 0)
+    float zhi, zlo;   // sum 2^(l a - K) as a df
+    int arg;          // lowest argmax (T = 0)
+};
+struct SlotRec {
+    df rho, w, h, r;
+    float cval;       // residual scale c = w_i Z_q / Z_p of slot i's sweep item
+    int x;
+    float lq, lp;     // the draft and target logits at x_i
+};
+struct StreamRec {
+    int32_t status, N, greedy, tau, n_pass, bonus;
     float a_hi, a_lo;
+    uint8_t pass[SPEC_MAX_KMAX + 4];   // sweep items: slots, candidates in descending order, then 0
 };
+struct SweepItem {   // one claim of the residual sweep, self-contained (32 bytes)
+    int32_t b;        // stream
+    int16_t slot;     // slot i of the item (N: the bonus row)
+    int16_t s0;       // first segment of the claim
+    float Kq, Kp;     // reference exponents of the draft and target rows at slot i
+    float cc;         // residual scale c = w_i Z_q / Z_p (1 for the bonus row)
+    float ah, al;     // a = log2(e) / T
+    int32_t bonus;    // 1: the bonus row's own mass, not a residual
+};
+constexpr size_t kHeaderBytes = 256;
+constexpr size_t kRowBytes = 1536;
+constexpr int kOffStatsCount = 0;    // u32: stats pieces published for this row
+constexpr int kOffSweepCount = 4;    // u32 (stream's first row): sweep segments published
+constexpr int kOffSweepTimeout = 8;  // u32 (stream's first row): a sweep wait gave up
+constexpr int kOffParts = 16;
+constexpr int kOffSeg = kOffParts + kPiecesMax * (int)sizeof(Part);
+constexpr int kOffRow = kOffSeg + kSegs * (int)sizeof(float);
+constexpr int kOffSlot = kOffRow + (int)sizeof(RowStat);
+constexpr int kOffStream = kOffSlot + (int)sizeof(SlotRec);
+static_assert(sizeof(WsHeader) <= kHeaderBytes, "header");
+static_assert(kOffStream + sizeof(StreamRec) <= kRowBytes, "row block");
+static_assert(kOffSlot % 8 == 0 && kOffRow % 16 == 0 && kOffParts % 16 == 0, "alignment");
 
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+__host__ __device__ inline size_t workspace_rows(int32_t B, int32_t kmax) {
+    return (size_t)B * (size_t)(2 * kmax + 1);
 }
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+__host__ __device__ inline size_t work_list_claims(int32_t B, int32_t kmax) {
+    return (size_t)B * (size_t)(kmax + 1) * (size_t)((kSegs + kSegsPerClaim - 1) / kSegsPerClaim);
 }
-__device__ __forceinline__ void cluster_sync_all() {
-    cluster_arrive();
-    cluster_wait();
+__host__ __device__ inline size_t workspace_bytes(int32_t B, int32_t kmax) {
+    if (B == 0) return 0;   // nothing is launched
+    return kHeaderBytes + workspace_rows(B, kmax) * kRowBytes + work_list_claims(B, kmax) * sizeof(SweepItem);
 }
+__device__ __forceinline__ WsHeader* ws_header(const VerifyParams& p) { return reinterpret_cast<WsHeader*>(p.ws); }
+__device__ __forceinline__ char* row_block(const VerifyParams& p, int64_t rho) {
+    return p.ws + kHeaderBytes + rho * (int64_t)kRowBytes;
+}
+template <typename T>
+__device__ __forceinline__ T* blk_at(char* blk, int off) {
+    return reinterpret_cast<T*>(blk + off);
+}
+__device__ __forceinline__ SweepItem* work_list(const VerifyParams& p) { return reinterpret_cast<SweepItem*>(p.list); }
 
-// ---------------------------------------------------------------------------------------
-// Chunk feeds.  A stage is U chunks per lane of up to two rows (q and p): lane L of a warp
-// takes chunks rel + u*32 + L, u < U.  The vector path (E = 8, 16-byte aligned rows) moves a
-// stage with one TMA bulk copy per row into a per-warp shared-memory ring of D stages, each
-// completing on its own mbarrier (one elected lane issues, every lane waits with a bounded
-// poll); the plain path (E = 1) loads directly.
-// ---------------------------------------------------------------------------------------
 constexpr int kSpinLimit = 1 << 20;   // mbarrier polls before a wait gives up (status TIMEOUT)
-
-// Row counters: a stats warp publishes a partial, then adds 1 to its row's counter with
-// release semantics; a verify CTA reads the partials of a row once the counter (read with
-// acquire semantics) equals the row's piece count.  The wait gives up after kRowWaitNs of
-// device time (or a value above the count, which only a non-zero workspace can hold).
-constexpr unsigned long long kRowWaitNs = 4000000000ull;
-
-__device__ __forceinline__ void count_release(unsigned* c) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c) : "memory");
-}
-__device__ __forceinline__ unsigned load_acquire(const unsigned* c) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
-    return v;
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ bool wait_count(const unsigned* c, unsigned want) {
-    const unsigned long long t0 = global_ns();
-    for (int it = 0; it < (1 << 26); ++it) {
-        const unsigned v = load_acquire(c);
-        if (v == want) return true;
-        if (v > want || global_ns() - t0 > kRowWaitNs) return false;
-        __nanosleep(64);
-    }
-    return false;
-}
-
-template <typename DQ, typename DP, int E>
-struct Feed;
-
-template <typename DQ, typename DP>
-struct Feed<DQ, DP, 8> {
-    static constexpr int BQ = 8 * (int)sizeof(DQ);
-    static constexpr int BP = 8 * (int)sizeof(DP);
-    static constexpr int U = (2 * 32 * (BQ + BP) <= 2048) ? 2 : 1;
-    static constexpr int GRP = 32 * U;                       // chunks per stage
-    static constexpr int ROWQ = GRP * BQ, ROWP = GRP * BP;
-    static constexpr int STAGE = ROWQ + ROWP;
-    static constexpr int DR = (kRingBytesPerCta / kWarps - 64) / STAGE;
-    static constexpr int D = DR < 2 ? 2 : (DR > 8 ? 8 : DR);
-    static constexpr int RING = D * STAGE + 64;              // bytes per warp (stages + barriers)
-    char* base;
-    uint64_t* bar;
-    int lane;
-    unsigned phase;     // parity of the next completion of each slot
-    unsigned pending;   // slots with a stage issued and not yet waited for
-    bool timeout;
-    __device__ __forceinline__ void init(char* b, int ln) {
-        base = b;
-        bar = reinterpret_cast<uint64_t*>(b + D * STAGE);
-        lane = ln;
-        phase = 0;
-        pending = 0;
-        timeout = false;
-        if (lane == 0) {
-            for (int i = 0; i < D; ++i) mbar_init(&bar[i], 1);
-            mbar_init_fence();
-        }
-        __syncwarp();
-    }
-    // segment start of a row (bytes), or null
-    __device__ __forceinline__ const char* seg_q(const void* row, int64_t c0) const {
-        return row ? reinterpret_cast<const char*>(row) + c0 * BQ : nullptr;
-    }
-    __device__ __forceinline__ const char* seg_p(const void* row, int64_t c0) const {
-        return reinterpret_cast<const char*>(row) + c0 * BP;
-    }
-    // stage of chunks [rel, rel + GRP) of the segment (nrel chunks long) into ring slot `slot`
-    __device__ __forceinline__ void issue(int slot, const char* gq, const char* gp, int rel, int nrel) {
-        if (timeout) return;   // after a failed wait nothing new is put in flight
-        pending |= 1u << slot;
-        __syncwarp();          // every lane is done reading this slot's previous stage
-        if (lane == 0) {
-            const int n = min(GRP, nrel - rel);
-            fence_proxy_async_smem();
-            mbar_expect_tx(&bar[slot], (unsigned)(n * ((gq ? BQ : 0) + BP)));
-            if (gq) bulk_g2s(base + slot * STAGE, gq + (size_t)rel * BQ, (unsigned)(n * BQ), &bar[slot]);
-            bulk_g2s(base + slot * STAGE + ROWQ, gp + (size_t)rel * BP, (unsigned)(n * BP), &bar[slot]);
-        }
-    }
-    __device__ __forceinline__ void wait(int slot) {
-        if (timeout) return;
-        const unsigned parity = (phase >> slot) & 1u;
-        int n = 0;
-        while (!mbar_try_wait(&bar[slot], parity)) {
-            if (++n > kSpinLimit) {
-                timeout = true;   // the slot stays pending; drain() waits for it once more
-                return;
-            }
-        }
-        phase ^= 1u << slot;
-        pending &= ~(1u << slot);
-    }
-    // before the CTA exits: wait (bounded) for any copy still in flight after a failed wait
-    __device__ __forceinline__ void drain() {
-        for (int slot = 0; slot < D; ++slot) {
-            if (!((pending >> slot) & 1u)) continue;
-            const unsigned parity = (phase >> slot) & 1u;
-            for (int n = 0; n < kSpinLimit && !mbar_try_wait(&bar[slot], parity); ++n) {
-            }
-        }
-    }
-    __device__ __forceinline__ void get(int slot, int u, const void*, const void*, int64_t, bool has_q,
-                                        float (&xq)[8], float (&xp)[8]) const {
-        const char* sq = base + slot * STAGE + (u * 32 + lane) * BQ;
-        const char* sp = base + slot * STAGE + ROWQ + (u * 32 + lane) * BP;
-        if (has_q) unpack<DQ>(sq, xq);
-        unpack<DP>(sp, xp);
-    }
-    template <typename T>
-    __device__ __forceinline__ static void unpack(const char* s, float (&x)[8]) {
-        if (sizeof(T) == 2) {
-            const uint4 v = *reinterpret_cast<const uint4*>(s);
-            x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
-            x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
-        } else {
-            const float4 a = *reinterpret_cast<const float4*>(s);
-            const float4 b = *reinterpret_cast<const float4*>(s + 16);
-            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-            x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-        }
-    }
-};
-
-template <typename DQ, typename DP>
-struct Feed<DQ, DP, 1> {
-    static constexpr int U = 4;
-    static constexpr int GRP = 32 * U;
-    static constexpr int D = 1;
-    static constexpr int RING = 0;
-    int lane;
-    bool timeout;
-    __device__ __forceinline__ void init(char*, int ln) {
-        lane = ln;
-        timeout = false;
-    }
-    __device__ __forceinline__ const char* seg_q(const void*, int64_t) const { return nullptr; }
-    __device__ __forceinline__ const char* seg_p(const void*, int64_t) const { return nullptr; }
-    __device__ __forceinline__ void issue(int, const char*, const char*, int, int) {}
-    __device__ __forceinline__ void wait(int) {}
-    __device__ __forceinline__ void drain() {}
-    __device__ __forceinline__ void get(int, int, const void* rq, const void* rp, int64_t k, bool has_q,
-                                        float (&xq)[1], float (&xp)[1]) const {
-        if (has_q) xq[0] = load_elem<DQ>(rq, k);
-        xp[0] = load_elem<DP>(rp, k);
-    }
-};
+constexpr int kStatsTimeout = -2;     // idx of a partial whose piece lost a bounded wait
 
 // ---------------------------------------------------------------------------------------
 // Per-lane accumulators
@@ -490,65 +352,6 @@ __device__ __forceinline__ float target_chunk_sum(const float (&xp)[E], float Kp
     LaneSum t;
     t.K = Kp;
     return t.terms<E>(xp, ah, al);
-}
-
-// ---------------------------------------------------------------------------------------
-// Warp sweep over this warp's segment [c0, c1) of a list of items (a row or a row pair),
-// each split into groups of U * 32 chunks; the ring runs D - 1 groups ahead of the consumer.
-// rows(it, rq, rp) gives an item's rows; begin(it) / consume(k, xq, xp) / end(it) see the
-// items in order.
-// ---------------------------------------------------------------------------------------
-template <typename DQ, typename DP, int E, typename RowsFn, typename BeginFn, typename ConsumeFn, typename EndFn,
-          typename FlushFn>
-__device__ __forceinline__ void sweep(Feed<DQ, DP, E>& feed, int items, int64_t c0, int64_t c1, int lane,
-                                      RowsFn rows, BeginFn begin_item, ConsumeFn consume, EndFn end_item,
-                                      FlushFn flush) {
-    constexpr int D = Feed<DQ, DP, E>::D;
-    constexpr int U = Feed<DQ, DP, E>::U;
-    const int G = (c1 > c0) ? (int)((c1 - c0 + 32 * U - 1) / (32 * U)) : 0;
-    const int nrel = (int)(c1 - c0);
-    int ii = 0, gi = 0, slot_i = 0;
-    const char *iq = nullptr, *ip = nullptr;
-    auto load_rows = [&](int it) {
-        const void *rq, *rp;
-        rows(it, rq, rp);
-        iq = feed.seg_q(rq, c0);
-        ip = feed.seg_p(rp, c0);
-    };
-    if (G > 0 && items > 0) load_rows(0);
-    auto issue_next = [&]() {
-        if (ii < items) feed.issue(slot_i, iq, ip, gi * 32 * U, nrel);
-        if (++slot_i == D) slot_i = 0;
-        if (++gi == G) {
-            gi = 0;
-            ++ii;
-            if (ii < items) load_rows(ii);
-        }
-    };
-    if (G > 0)
-        for (int s = 0; s < D - 1; ++s) issue_next();
-    int slot_c = 0;
-    for (int it = 0; it < items; ++it) {
-        const void *cq, *cp;
-        rows(it, cq, cp);
-        begin_item(it);
-        for (int g = 0; g < G; ++g) {
-            issue_next();
-            feed.wait(slot_c);
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t k = c0 + ((int64_t)g * U + u) * 32 + lane;
-                if (k < c1) {
-                    float xq[E], xp[E];
-                    feed.get(slot_c, u, cq, cp, k, cq != nullptr, xq, xp);
-                    consume(k, xq, xp);
-                }
-            }
-            flush();   // one group of chunks done
-            if (++slot_c == D) slot_c = 0;
-        }
-        end_item(it);
-    }
 }
 
 // Fixed-point weight (times `scale`) of each element of one chunk pair.
@@ -751,26 +554,17 @@ __device__ int valid_prefix(const VerifyParams& p) {
     return L;
 }
 
-// Chunks per warp of the stats kernel: equal shares of all rows' chunks, but at least
-// ceil(n / (kPiecesMax - 2)) so that no row is cut into more than kPiecesMax pieces.
-__device__ __forceinline__ int64_t stats_share(int64_t rows, int64_t n, int64_t nw) {
-    const int64_t lw = (rows * n + nw - 1) / nw;
-    const int64_t lmin = (n + kPiecesMax - 3) / (kPiecesMax - 2);
-    return lw > lmin ? lw : (lmin > 0 ? lmin : 1);
-}
+// ---------------------------------------------------------------------------------------
+// stats_kernel
+// ---------------------------------------------------------------------------------------
+// 16-byte rows (E = 8): each warp owns a ring of kStages stages of kStageBytes in shared
+// memory, each filled by one TMA bulk copy (issued by lane 0) that completes on the stage's
+// mbarrier; every lane waits with a bounded poll.
+constexpr int kStages = 4;
+constexpr int kStageBytes = 2048;
+constexpr int kStatsRingBytes = kStatsWarps * kStages * kStageBytes;
+static size_t stats_smem_bytes(int E) { return E == 8 ? (size_t)kStatsRingBytes : 0; }
 
-// ---------------------------------------------------------------------------------------
-// Stats kernel: every logit of the batch is read once.
-//
-// Rows are numbered stream by stream: stream b owns rows [g_b, g_b + 2 N_b + 1), g_b =
-// 2 cu[b] + b; its target rows 0..N_b come first, then its draft rows 0..N_b-1.  The chunks
-// of all these rows, end to end, are cut into equal contiguous shares, one per warp of a
-// persistent grid, so every warp streams the same number of bytes, from one row or a few
-// consecutive ones.  Per row piece a warp leaves one partial: (reference K, sum 2^(l a - K))
-// for T > 0, (max, lowest argmax) for T = 0; the partial of piece k of row rho sits at
-// rho * kPiecesMax + k.  Draft rows of greedy streams and all rows of a stream with an
-// invalid temperature are skipped (never read).
-// ---------------------------------------------------------------------------------------
 template <typename T, int E, typename AddFn>
 __device__ __forceinline__ void stream_piece(const void* row, int64_t c0, int64_t c1, int lane, AddFn add) {
     constexpr int U = (E == 8) ? (sizeof(T) == 2 ? 4 : 2) : 8;   // 64 bytes per lane and batch
@@ -805,88 +599,10 @@ __device__ __forceinline__ void stream_piece(const void* row, int64_t c0, int64_
     }
 }
 
-// 16-byte rows (E = 8): each lane copies its own chunks into a per-warp ring of kStages
-// stages of 2 KB with cp.async and later reads back only those chunks, so the ring needs no
-// synchronisation beyond each thread's own wait_group; kStages - 1 stages are in flight while
-// one is summed.  A float32 chunk (32 bytes) is stored as two 16-byte planes.
-constexpr int kStages = 4;
-constexpr int kStageBytes = 2048;
-constexpr int kStatsRingBytes = kWarps * kStages * kStageBytes;
-static size_t stats_smem_bytes(int E) { return E == 8 ? (size_t)kStatsRingBytes : 0; }
-
-template <typename T, typename AddFn, typename GroupFn>
-__device__ __forceinline__ void stream_piece_ring(char* ring, const void* row, int64_t c0, int64_t c1, int lane,
-                                                  AddFn add, GroupFn add_full) {
-    constexpr int BT = 8 * (int)sizeof(T);   // bytes per chunk
-    constexpr int G = kStageBytes / BT;      // chunks per stage
-    constexpr int U = G / 32;                // chunks per lane and stage
-    constexpr int LPC = BT / 16;             // 16-byte copies per chunk
-    const char* g = reinterpret_cast<const char*>(row);
-    const int64_t nb = (c1 - c0 + G - 1) / G;
-    auto issue = [&](int64_t i, int slot) {
-        if (i < nb) {
-            char* st = ring + slot * kStageBytes;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t k = c0 + i * G + u * 32 + lane;
-                if (k < c1)
-#pragma unroll
-                    for (int l = 0; l < LPC; ++l) cp_async16(st + l * (G * 16) + (u * 32 + lane) * 16, g + k * BT + 16 * l);
-            }
-        }
-        cp_async_commit();   // an empty group keeps the group count in step
-    };
-#pragma unroll
-    for (int i = 0; i < kStages - 1; ++i) issue(i, i);
-    int slot = 0;
-    for (int64_t i = 0; i < nb; ++i) {
-        issue(i + kStages - 1, slot == 0 ? kStages - 1 : slot - 1);
-        cp_async_wait<kStages - 1>();
-        const char* st = ring + slot * kStageBytes;
-        if (c0 + (i + 1) * G <= c1) {   // a full stage: every lane has all U chunks
-            float x[U][8];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if constexpr (sizeof(T) == 2) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(st + (u * 32 + lane) * 16);
-                    x[u][0] = bf16_lo(v.x); x[u][1] = bf16_hi(v.x); x[u][2] = bf16_lo(v.y); x[u][3] = bf16_hi(v.y);
-                    x[u][4] = bf16_lo(v.z); x[u][5] = bf16_hi(v.z); x[u][6] = bf16_lo(v.w); x[u][7] = bf16_hi(v.w);
-                } else {
-                    const float4 a = *reinterpret_cast<const float4*>(st + (u * 32 + lane) * 16);
-                    const float4 b = *reinterpret_cast<const float4*>(st + G * 16 + (u * 32 + lane) * 16);
-                    x[u][0] = a.x; x[u][1] = a.y; x[u][2] = a.z; x[u][3] = a.w;
-                    x[u][4] = b.x; x[u][5] = b.y; x[u][6] = b.z; x[u][7] = b.w;
-                }
-            }
-            add_full(x, c0 + i * G + lane);
-            slot = (slot + 1 == kStages) ? 0 : slot + 1;
-            continue;
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t k = c0 + i * G + u * 32 + lane;
-            if (k < c1) {
-                float x[8];
-                if constexpr (sizeof(T) == 2) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(st + (u * 32 + lane) * 16);
-                    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
-                    x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
-                } else {
-                    const float4 a = *reinterpret_cast<const float4*>(st + (u * 32 + lane) * 16);
-                    const float4 b = *reinterpret_cast<const float4*>(st + G * 16 + (u * 32 + lane) * 16);
-                    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-                    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-                }
-                add(x, k * 8);
-            }
-        }
-        slot = (slot + 1 == kStages) ? 0 : slot + 1;
-    }
-}
-
 // The stats kernel's per-warp ring: kStages stages of kStageBytes in shared memory, each
-// filled by one TMA bulk copy (issued by lane 0) that completes on the stage's mbarrier; every
-// lane waits with a bounded poll.  One instruction per stage moves the data, so the scan's
+// filled by one TMA bulk copy (issued by lane 0, with an evict-first L2 policy: the logits are
+// streamed through once and must not push the kernels' code and workspace out of L2) that
+// completes on the stage's mbarrier; every lane waits with a bounded poll.  One instruction per stage moves the data, so the scan's
 // issue slots go to the arithmetic.  Slots and phases persist from piece to piece.
 struct StatsRing {
     char* base;
@@ -915,7 +631,7 @@ struct StatsRing {
         if (lane == 0) {
             fence_proxy_async_smem();
             mbar_expect_tx(&bar[slot], bytes);
-            bulk_g2s(base + slot * kStageBytes, src, bytes, &bar[slot]);
+            bulk_g2s_hint(base + slot * kStageBytes, src, bytes, &bar[slot], l2_evict_first_policy());
         }
     }
     __device__ __forceinline__ void wait(int slot) {
@@ -942,10 +658,12 @@ struct StatsRing {
 };
 
 // One piece [c0, c1) of a 16-byte aligned row through the bulk ring: full stages go to
-// add_full (U chunks per lane), the ragged last stage chunk by chunk to add.
-template <typename T, typename AddFn, typename GroupFn>
+// add_full (U chunks per lane), the ragged last stage chunk by chunk to add.  after_last() runs
+// (in every lane) right after the piece's last copy has been issued, while D - 1 stages are
+// still to be consumed: the next claim is fired there, so its round trip overlaps this tail.
+template <typename T, typename AddFn, typename GroupFn, typename AfterFn>
 __device__ __forceinline__ void stream_piece_bulk(StatsRing& R, const void* row, int64_t c0, int64_t c1, int lane,
-                                                  AddFn add, GroupFn add_full) {
+                                                  AddFn add, GroupFn add_full, AfterFn after_last) {
     constexpr int BT = 8 * (int)sizeof(T);   // bytes per chunk
     constexpr int G = kStageBytes / BT;      // chunks per stage
     constexpr int U = G / 32;                // chunks per lane and stage
@@ -953,7 +671,10 @@ __device__ __forceinline__ void stream_piece_bulk(StatsRing& R, const void* row,
     const int64_t n = c1 - c0;
     const int nb = (int)((n + G - 1) / G);
     auto issue = [&](int i) {
-        if (i < nb) R.issue(i % kStages, g + (int64_t)i * G * BT, (unsigned)(min((int64_t)G, n - (int64_t)i * G) * BT));
+        if (i < nb) {
+            R.issue(i % kStages, g + (int64_t)i * G * BT, (unsigned)(min((int64_t)G, n - (int64_t)i * G) * BT));
+            if (i == nb - 1) after_last();
+        }
     };
 #pragma unroll
     for (int i = 0; i < kStages - 1; ++i) issue(i);
@@ -1000,11 +721,9 @@ __device__ __forceinline__ void stream_piece_bulk(StatsRing& R, const void* row,
     }
 }
 
-constexpr int kStatsTimeout = -2;   // idx of a partial whose stats piece lost a bounded wait
-
-template <typename T, int E>
+template <typename T, int E, typename AfterFn>
 __device__ __forceinline__ void stats_piece(StatsRing& ring, const void* row, int64_t c0, int64_t c1, bool greedy,
-                                            float ah, float al, int lane, Part* dst) {
+                                            float ah, float al, int lane, Part* dst, AfterFn after_last) {
     constexpr int UG = kStageBytes / (8 * (int)sizeof(T)) / 32;   // chunks per lane and stage
     if (greedy) {
         LaneMax mx;
@@ -1014,52 +733,94 @@ __device__ __forceinline__ void stats_piece(StatsRing& ring, const void* row, in
 #pragma unroll
             for (int u = 0; u < UG; ++u) mx.add<8>(x[u], (k0 + 32 * u) * 8);
         };
-        if constexpr (E == 8) stream_piece_bulk<T>(ring, row, c0, c1, lane, f, g);
-        else stream_piece<T, E>(row, c0, c1, lane, f);
+        if constexpr (E == 8) {
+            stream_piece_bulk<T>(ring, row, c0, c1, lane, f, g, after_last);
+        } else {
+            after_last();
+            stream_piece<T, E>(row, c0, c1, lane, f);
+        }
         mx.publish(dst, lane);
         if (ring.timeout && lane == 0) dst->idx = kStatsTimeout;
     } else {
         LaneSum sum;
         auto f = [&](const float (&x)[E], int64_t) { sum.add<E>(x, ah, al); };
         auto g = [&](const float (&x)[UG][8], int64_t) { sum.add_group<UG>(x, ah, al); };
-        if constexpr (E == 8) stream_piece_bulk<T>(ring, row, c0, c1, lane, f, g);
-        else stream_piece<T, E>(row, c0, c1, lane, f);
+        if constexpr (E == 8) {
+            stream_piece_bulk<T>(ring, row, c0, c1, lane, f, g, after_last);
+        } else {
+            after_last();
+            stream_piece<T, E>(row, c0, c1, lane, f);
+        }
         sum.publish(dst, lane);
         if (ring.timeout && lane == 0) dst->idx = kStatsTimeout;
     }
 }
 
-template <typename DQ, typename DP, int E>
-__global__ void __launch_bounds__(kThreads, 3) stats_kernel(const VerifyParams p) {
-    extern __shared__ __align__(16) char stats_smem[];
-    // the verify kernel may be scheduled now: it reads a row's partials once its counter is full
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __shared__ __align__(8) uint64_t stats_bars[kWarps][kStages];
-    const int lane = threadIdx.x & 31;
-    StatsRing ring;
-    ring.init(stats_smem + (threadIdx.x >> 5) * (kStages * kStageBytes), stats_bars[threadIdx.x >> 5], lane);
-    const int L = valid_prefix(p);
-    if (L == 0) return;
-    const int64_t n = p.nchunk;
-    const int64_t rows = 2 * (int64_t)p.cu[L] + L;
-    const int64_t lw = stats_share(rows, n, p.stats_warps);
-    const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    int64_t f = gw * lw;
-    const int64_t f1 = min(f + lw, rows * n);
-    if (f >= f1) return;
-    int64_t rho = f / n;
-    int64_t c = f - rho * n;
-    // the stream of the first row: largest b in [0, L) with g_b <= rho
-    int lo = 0, hi = L - 1;
+// a = log2(e) / T as a df
+__device__ __forceinline__ df scale_of_temperature(float T) {
+    const df l2e{1.4426950216293335f, 1.925963033500011e-08f};
+    return df_div(l2e, df_make(T));
+}
+
+__device__ __forceinline__ bool temperature_ok(float T) { return isfinite(T) && (T == 0.f || T >= FLT_MIN); }
+
+// The stream owning stats row rho: the largest b in [lo, L) with g_b = 2 cu[b] + b <= rho.
+__device__ __forceinline__ int stream_of_row(const VerifyParams& p, int64_t rho, int lo, int L) {
+    int hi = L - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (2 * (int64_t)p.cu[mid] + mid <= rho) lo = mid;
         else hi = mid - 1;
     }
-    int b = lo;
+    return lo;
+}
+
+// Chunks per warp of the stats kernel: equal shares of all rows' chunks, but at least
+// ceil(n / (kPiecesMax - 2)) so that no row is cut into more than kPiecesMax pieces.
+__host__ __device__ inline int64_t stats_share(int64_t rows, int64_t n, int64_t nw) {
+    const int64_t lw = (rows * n + nw - 1) / nw;
+    const int64_t lmin = (n + kPiecesMax - 3) / (kPiecesMax - 2);
+    return lw > lmin ? lw : (lmin > 0 ? lmin : 1);
+}
+// The pieces of stats row rho: warps first .. first + count - 1; warp gw's partial is piece
+// gw - first of the row.
+__device__ __forceinline__ void row_pieces(int64_t rho, int64_t n, int64_t lw, int64_t& first, int& count) {
+    first = rho * n / lw;
+    count = (int)((rho * n + n - 1) / lw - first) + 1;
+}
+
+template <typename DQ, typename DP, int E>
+__global__ void __launch_bounds__(kStatsThreads, 768 / kStatsThreads) stats_kernel(const VerifyParams p) {
+    extern __shared__ __align__(16) char stats_smem[];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ __align__(8) uint64_t stats_bars[kStatsWarps][kStages];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    StatsRing ring;
+    ring.init(stats_smem + warp * (kStages * kStageBytes), stats_bars[warp], lane);
+    const int L = valid_prefix(p);
+    WsHeader* hdr = ws_header(p);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        hdr->L = L;
+        // the sweep's work list starts empty in every call, whatever the workspace held (the
+        // decide kernel appends only after this grid has completed)
+        hdr->ticket_sweep = 0ull;
+        hdr->sweep_total = 0ull;
+    }
+    if (L == 0) return;
+    const int64_t n = p.nchunk;
+    const int64_t rows = 2 * (int64_t)p.cu[L] + L;
+    const int64_t lw = stats_share(rows, n, p.stats_warps);
+    const int64_t gw = (int64_t)blockIdx.x * kStatsWarps + warp;
+    int64_t f = gw * lw;
+    const int64_t f1 = min(f + lw, rows * n);
+    if (f >= f1) return;
+    int64_t rho = f / n;
+    int64_t c = f - rho * n;
+    int b = stream_of_row(p, rho, 0, L);
     int64_t gb = 2 * (int64_t)p.cu[b] + b;
     int Nb = p.cu[b + 1] - p.cu[b];
     const int64_t V = p.V;
+    auto nothing = []() {};
     while (f < f1) {
         const int64_t c_end = min(n, c + (f1 - f));
         while (rho - gb > 2 * (int64_t)Nb) {
@@ -1071,23 +832,23 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const VerifyParams p
         const float T = p.temp[b];
         const bool greedy = (T == 0.f);
         const bool draft = j > Nb;
-        const bool skip = !(isfinite(T) && (T == 0.f || T >= FLT_MIN)) || (draft && greedy);
+        const bool skip = !temperature_ok(T) || (draft && greedy);
         if (!skip) {
             float ah = 0.f, al = 0.f;
             if (!greedy) {
-                const df l2e{1.4426950216293335f, 1.925963033500011e-08f};
-                const df a = df_div(l2e, df_make(T));
+                const df a = scale_of_temperature(T);
                 ah = a.hi;
                 al = a.lo;
             }
-            Part* dst = row_parts(p, rho) + (gw - rho * n / lw);
+            char* blk = row_block(p, rho);
+            Part* dst = blk_at<Part>(blk, kOffParts) + (gw - rho * n / lw);
             if (draft)
-                stats_piece<DQ, E>(ring, row_ptr<DQ>(p.dq, (int64_t)p.cu[b] + (j - Nb - 1), V), c, c_end, false,
-                                   ah, al, lane, dst);
+                stats_piece<DQ, E>(ring, row_ptr<DQ>(p.dq, (int64_t)p.cu[b] + (j - Nb - 1), V), c, c_end, false, ah,
+                                   al, lane, dst, nothing);
             else
                 stats_piece<DP, E>(ring, row_ptr<DP>(p.dp, (int64_t)p.cu[b] + b + j, V), c, c_end, greedy, ah, al,
-                                   lane, dst);
-            if (lane == 0) count_release(row_counter(p, rho));   // lane 0 wrote the partial
+                                   lane, dst, nothing);
+            if (lane == 0) atomicAdd(blk_at<unsigned>(blk, kOffStatsCount), 1u);   // after lane 0's partial
         }
         f += c_end - c;
         c = 0;
@@ -1098,163 +859,121 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const VerifyParams p
 }
 
 // ---------------------------------------------------------------------------------------
-// The verify kernel (one cluster per stream)
+// decide_kernel: one CTA per stream
 // ---------------------------------------------------------------------------------------
-template <typename DQ, typename DP, int E>
-__global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams p) {
-    extern __shared__ __align__(16) char ring_smem[];
-    __shared__ Shared sh;
-    cg::cluster_group cluster = cg::this_cluster();
-    const int C = (int)cluster.num_blocks();
-    const int crank = (int)cluster.block_rank();
-    const int b = (int)(blockIdx.x / C);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nseg = C * kWarps;
-    const int64_t c0 = min(p.nchunk, (int64_t)(crank * kWarps + warp) * p.seg_chunks);
-    const int64_t c1 = min(p.nchunk, c0 + p.seg_chunks);
-    const int64_t V = p.V;
-    Feed<DQ, DP, E> feed;
-    feed.init(ring_smem + warp * Feed<DQ, DP, E>::RING, lane);
+// Part index of a stream's rows inside the per-stream kernels: draft row i -> i (i < N),
+// target row i -> N + i (i <= N); stats row of part r: g_b + N + 1 + r (draft), g_b + r - N
+// (target).
+__device__ __forceinline__ int64_t stats_row_of_part(int64_t gb, int N, int r) {
+    return gb + (r < N ? N + 1 + r : r - N);
+}
 
-    // ---- stream header (identical in every CTA): offsets, temperature, tokens, and the draft
-    // and target logits at each draft token (loaded now, consumed after the sweep)
-    const int base = p.cu[b];
-    const int n_raw = p.cu[b + 1] - base;
-    const int Lv = valid_prefix(p);   // streams from the first broken count on are invalid
-    const bool offsets_ok = b < Lv;
-    const int N = offsets_ok ? n_raw : 0;
+struct DecideShared {
+    float rowK[kMaxRows];
+    df rowZ[kMaxRows];
+    int rowArg[kMaxRows];
+    df rho[SPEC_MAX_KMAX];
+    df w[SPEC_MAX_KMAX + 1];
+    df u_acc[SPEC_MAX_KMAX + 1];
+    float cval[SPEC_MAX_KMAX + 1];
+    float lq[SPEC_MAX_KMAX], lp[SPEC_MAX_KMAX];
+    int x[SPEC_MAX_KMAX];
+    int pass_list[SPEC_MAX_KMAX + 1];
+    int n_pass, status, tau, bonus;
+    unsigned long long claim0;
+};
+
+template <typename DQ, typename DP>
+__global__ void __launch_bounds__(kThreads) decide_kernel(const VerifyParams p) {
+    __shared__ DecideShared sh;
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // ---- prologue (inputs only, overlaps the stats kernel): temperature, uniforms, and -
+    // once the stream's offsets are known to be valid - its tokens and the logits at them
     const float T = p.temp[b];
-    const bool temp_ok = isfinite(T) && (T == 0.f || T >= FLT_MIN);
+    const bool temp_ok = temperature_ok(T);
     const bool greedy = (T == 0.f);
-    const int64_t dbase = offsets_ok ? base : 0;
-    const int64_t tbase = dbase + b;
-    auto qrow = [&](int i) { return row_ptr<DQ>(p.dq, dbase + i, V); };
-    auto prow = [&](int i) { return row_ptr<DP>(p.dp, tbase + i, V); };
-    if (tid < kWarps) sh.to_flag[tid] = 0;
+    const df a = (temp_ok && !greedy) ? scale_of_temperature(T) : df{0.f, 0.f};
+    if (tid <= p.kmax && temp_ok && !greedy) {
+        const uint4 c = make_uint4((uint32_t)tid, (uint32_t)b, (uint32_t)p.step, (uint32_t)(p.step >> 32));
+        const uint4 wds = philox4x32_10(c, make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
+        sh.u_acc[tid] = uniform24_df(wds.x);
+    }
+    if (tid <= SPEC_MAX_KMAX) sh.w[tid] = df{__int_as_float(0x7fffffff), 0.f};
+    // stream b has valid offsets iff no stream j <= b breaks the packed layout
+    bool broken = false;
+    for (int j = tid; j <= b; j += kThreads) broken |= offsets_bad(p, j);
+    const bool offsets_ok = !__syncthreads_or(broken);
+    const int base = p.cu[b];
+    const int N = offsets_ok ? p.cu[b + 1] - base : 0;
+    const int64_t V = p.V;
     bool bad_tok = false;
     if (offsets_ok && temp_ok && tid < N) {
         const int xi = p.tokens[base + tid];
         sh.x[tid] = xi;
         bad_tok = (xi < 0 || xi >= p.V);
         if (!bad_tok && !greedy) {
-            sh.lq[tid] = load_elem<DQ>(qrow(tid), xi);
-            sh.lp[tid] = load_elem<DP>(prow(tid), xi);
+            sh.lq[tid] = load_elem<DQ>(row_ptr<DQ>(p.dq, (int64_t)base + tid, V), xi);
+            sh.lp[tid] = load_elem<DP>(row_ptr<DP>(p.dp, (int64_t)base + b + tid, V), xi);
         }
     }
     bad_tok = __syncthreads_or(bad_tok);
-    if (tid == 0) {
-        int st = SPEC_ST_OK;
-        if (!offsets_ok) st = SPEC_ST_BAD_OFFSETS;
-        else if (!temp_ok) st = SPEC_ST_BAD_TEMPERATURE;
-        else if (bad_tok) st = SPEC_ST_BAD_TOKEN;
-        sh.N = N;
-        sh.status = st;
-        sh.greedy = (st == SPEC_ST_OK && greedy);
-        float ah = 0.f, al = 0.f;
-        if (st == SPEC_ST_OK && T > 0.f) {   // a = log2(e) / T as a df
-            const df l2e{1.4426950216293335f, 1.925963033500011e-08f};
-            const df q = df_div(l2e, df_make(T));
-            ah = q.hi;
-            al = q.lo;
-        }
-        sh.a_hi = ah;
-        sh.a_lo = al;
-        sh.tau = 0;
-        sh.sample_seg = -1;
-        sh.sample_bonus = 0;
-        sh.n_pass = 0;
-    }
-    __syncthreads();
-    const float ah = sh.a_hi, al = sh.a_lo;
-    const int nrows = 2 * N + 1;   // part index: draft row i -> i, target row i -> N + i
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // Everything above read only the call's inputs.  The stats kernel writes every row of a
-    // stream with valid offsets and temperature (target rows only when greedy); each row is
-    // waited for here - also when the stream already failed, so that its counters can be reset
-    // at the end - and its partials are read once the row's counter is full.
-    // the per-slot uniforms depend on (seed, step, stream, slot) only
-    if (sh.status == SPEC_ST_OK && !greedy && tid <= N) {
-        const uint4 c = make_uint4((uint32_t)tid, (uint32_t)b, (uint32_t)p.step, (uint32_t)(p.step >> 32));
-        const uint4 wds = philox4x32_10(c, make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
-        sh.u_acc[tid] = uniform24_df(wds.x);
-        sh.u_smp[tid] = wds.y;
-        sh.h[tid] = df{__int_as_float(0x7fffffff), 0.f};
-        sh.r[tid] = df{__int_as_float(0x7fffffff), 0.f};
-    }
-    const bool rows_written = offsets_ok && temp_ok;
-    const int64_t nck = p.nchunk;
-    const int64_t lw = stats_share(2 * (int64_t)p.cu[Lv] + Lv, nck, p.stats_warps);
-    // stats row of part r: target row i at g_b + i, draft row i at g_b + N + 1 + i
-    auto stats_row = [&](int r) { return 2 * (int64_t)base + b + (r < N ? N + 1 + r : r - N); };
+    WsHeader* hdr = ws_header(p);
+    if (!offsets_ok) return;   // finish_kernel reports BAD_OFFSETS
+    const int L = __ldcg(&hdr->L);
+    const int64_t lw = stats_share(2 * (int64_t)p.cu[L] + L, p.nchunk, p.stats_warps);
+    const int64_t gb = 2 * (int64_t)base + b;
+    const int nrows = 2 * N + 1;
+    const bool reduce_rows = temp_ok && !bad_tok;
+
+    // ---- row statistics from the pieces' partials: one warp per row, lane l holds piece l
+    // (same order every time, so the result is reproducible bit for bit)
     bool stats_to = false;
-    if (rows_written) {
-        // one row per half-warp (16 rows per pass): lane l of a half holds pieces l, l + 16, ...
-        const bool ok = sh.status == SPEC_ST_OK;
-        const int hl = lane & 15;
-        for (int r0 = (greedy ? N : 0) + 2 * warp; r0 < nrows; r0 += 2 * kWarps) {
-            const int r = r0 + (lane >> 4);
-            const bool have = r < nrows;
-            int cnt = 0;
-            bool full = false;
-            int64_t rho = 0;
-            if (have) {
-                rho = stats_row(r);
-                const int64_t first = rho * nck / lw;
-                cnt = (int)((rho * nck + nck - 1) / lw - first) + 1;   // pieces of this row
-                full = wait_count(row_counter(p, rho), (unsigned)cnt);
-                stats_to |= !full;
-            }
-            if (!ok) continue;
-            // row statistics from the per-piece partials (same order in every CTA, so every
-            // CTA holds bit-identical values)
-            constexpr int kSlots = kPiecesMax / 16;
-            Part e[kSlots];
+    if (temp_ok) {
+        for (int r = (greedy ? N : 0) + warp; r < nrows; r += kWarps) {
+            const int64_t rho = stats_row_of_part(gb, N, r);
+            char* blk = row_block(p, rho);
+            int64_t first;
+            int cnt_want;
+            row_pieces(rho, p.nchunk, lw, first, cnt_want);
+            const unsigned cnt = __ldcg(blk_at<unsigned>(blk, kOffStatsCount));
+            Part e[2];
 #pragma unroll
-            for (int k = 0; k < kSlots; ++k) {
-                const int pk = hl + 16 * k;
-                if (have && full && pk < cnt) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(row_parts(p, rho) + pk));
+            for (int k = 0; k < 2; ++k) {
+                const int pk = lane + 32 * k;
+                e[k] = Part{greedy ? -kInf : kNoRef, 0.f, 0.f, INT_MAX};
+                if (pk < cnt_want) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(blk_at<Part>(blk, kOffParts) + pk));
                     e[k] = Part{v.x, v.y, v.z, __float_as_int(v.w)};
-                } else {
-                    e[k] = Part{greedy ? -kInf : kNoRef, 0.f, 0.f, INT_MAX};
                 }
-                stats_to |= (e[k].idx == kStatsTimeout);   // that piece's bounded wait gave up
             }
+            const bool full = (cnt == (unsigned)cnt_want);
+            stats_to |= __any_sync(0xffffffffu, !full || e[0].idx == kStatsTimeout || e[1].idx == kStatsTimeout);
+            if (!reduce_rows || !full) continue;
             if (greedy) {
-                float Kr = e[0].K;
-#pragma unroll
-                for (int k = 1; k < kSlots; ++k) Kr = fmax_nan(Kr, e[k].K);
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) Kr = fmax_nan(Kr, __shfl_xor_sync(0xffffffffu, Kr, o));
-                int arg = INT_MAX;
-#pragma unroll
-                for (int k = 0; k < kSlots; ++k) arg = min(arg, e[k].K == Kr ? e[k].idx : INT_MAX);
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) arg = min(arg, __shfl_xor_sync(0xffffffffu, arg, o));
-                if (have && hl == 0) {
+                const float Kr = warp_max_nan(fmax_nan(e[0].K, e[1].K));
+                const int arg = warp_min_i(min(e[0].K == Kr ? e[0].idx : INT_MAX, e[1].K == Kr ? e[1].idx : INT_MAX));
+                if (lane == 0) {
                     sh.rowK[r] = Kr;
                     sh.rowArg[r] = arg;
                     sh.rowZ[r] = df{0.f, 0.f};
                 }
                 continue;
             }
-            float Kr = e[0].K;
-#pragma unroll
-            for (int k = 1; k < kSlots; ++k) Kr = fmaxf(Kr, e[k].K);
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) Kr = fmaxf(Kr, __shfl_xor_sync(0xffffffffu, Kr, o));
+            const float Kr = warp_max(fmaxf(e[0].K, e[1].K));
             df z{0.f, 0.f};
 #pragma unroll
-            for (int k = 0; k < kSlots; ++k) {
-                const float sc = (e[k].K == Kr) ? 1.f : pow2_int(e[k].K - Kr);
-                z = df_add(z, df_scale(df{e[k].s_hi, e[k].s_lo}, sc));
-            }
+            for (int k = 0; k < 2; ++k)
+                z = df_add(z, df_scale(df{e[k].s_hi, e[k].s_lo}, (e[k].K == Kr) ? 1.f : pow2_int(e[k].K - Kr)));
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) {
+            for (int o = 16; o > 0; o >>= 1) {
                 const df other{__shfl_xor_sync(0xffffffffu, z.hi, o), __shfl_xor_sync(0xffffffffu, z.lo, o)};
                 z = df_add(z, other);
             }
-            if (have && hl == 0) {
+            if (lane == 0) {
                 sh.rowK[r] = Kr;
                 sh.rowZ[r] = z;
                 sh.rowArg[r] = INT_MAX;
@@ -1262,13 +981,24 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
         }
     }
     stats_to = __syncthreads_or(stats_to);
-    if (tid == 0 && stats_to) {
-        if (sh.status == SPEC_ST_OK) sh.status = SPEC_ST_TIMEOUT;
-        sh.to_flag[0] = 1;   // the time-bounded waits of the cluster's CTAs may end differently
+    // the stream's counters go back to zero for the next call (every row, read or not)
+    for (int r = tid; r < nrows; r += kThreads) *blk_at<unsigned>(row_block(p, gb + r), kOffStatsCount) = 0u;
+    if (tid == 0) {
+        *blk_at<unsigned>(row_block(p, gb), kOffSweepCount) = 0u;
+        *blk_at<unsigned>(row_block(p, gb), kOffSweepTimeout) = 0u;
+        int st = SPEC_ST_OK;
+        if (!temp_ok) st = SPEC_ST_BAD_TEMPERATURE;
+        else if (bad_tok) st = SPEC_ST_BAD_TOKEN;
+        else if (stats_to) st = SPEC_ST_TIMEOUT;
+        sh.status = st;
+        sh.tau = 0;
+        sh.n_pass = 0;
+        sh.bonus = 0;
     }
     __syncthreads();
+
+    // ---- validity of the rows read, q_i(x_i) > 0, per-slot ratios
     if (sh.status == SPEC_ST_OK) {
-        // ---- validity of the rows read, q_i(x_i) > 0, per-slot ratios
         bool bad_row = false, zero_q = false;
         for (int r = (greedy ? N : 0) + tid; r < nrows; r += kThreads) {
             const float K = sh.rowK[r];
@@ -1281,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
             const float Kq = sh.rowK[tid], Kp = sh.rowK[N + tid];
             df rho{0.f, 0.f};
             if (!zero_q && isfinite(lq) && isfinite(lp) && isfinite(Kq) && isfinite(Kp)) {
-                const df e = df_sub(exponent_df(lp, ah, al, Kp), exponent_df(lq, ah, al, Kq));
+                const df e = df_sub(exponent_df(lp, a.hi, a.lo, Kp), exponent_df(lq, a.hi, a.lo, Kq));
                 rho = df_div(df_mul(df_exp2(e), sh.rowZ[tid]), sh.rowZ[N + tid]);
             }
             sh.rho[tid] = rho;
@@ -1295,172 +1025,518 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
         __syncthreads();
     }
 
-    const df one{1.f, 0.f};
-    int np = 0;
     // ---- decisions
-    if (sh.status == SPEC_ST_OK && greedy) {
-        if (tid == 0) {
-            int tau = N;
+    const df one{1.f, 0.f};
+    if (tid == 0 && sh.status == SPEC_ST_OK) {
+        int n = 0, tau = 0;
+        if (greedy) {
+            tau = N;
             for (int i = 0; i < N; ++i)
                 if (sh.rowArg[N + i] != sh.x[i]) {
                     tau = i;
                     break;
                 }
+        } else if (p.rule == 1) {
+            sh.w[0] = one;
+            for (int i = 0; i < N; ++i) sh.w[i + 1] = df_min(one, df_mul(sh.w[i], sh.rho[i]));
+            if (N > 0 && df_le(sh.u_acc[N - 1], sh.w[N])) {
+                tau = N;   // eta_N <= w_N = h_N: accept everything, no residual needed
+            } else {
+                for (int i = N - 1; i >= 1; --i)   // candidates: eta_i <= w_i (h_i <= w_i)
+                    if (df_le(sh.u_acc[i - 1], sh.w[i])) sh.pass_list[n++] = i;
+                if (N > 0) sh.pass_list[n++] = 0;
+            }
+        } else {
+            tau = N;
+            for (int i = 0; i < N; ++i)
+                if (!df_le(sh.u_acc[i], df_min(one, sh.rho[i]))) {
+                    tau = i;
+                    break;
+                }
+            if (tau < N) {
+                sh.w[tau] = one;
+                sh.pass_list[n++] = tau;
+            }
+        }
+        if (!greedy && tau == N) {   // every draft accepted: the sweep sums the bonus row instead
+            sh.pass_list[0] = N;
+            n = 1;
+            sh.bonus = 1;
+        }
+        sh.tau = tau;
+        sh.n_pass = n;
+    }
+    __syncthreads();
+    int np = sh.n_pass;
+    if (tid < np && !sh.bonus) {
+        const int i = sh.pass_list[tid];
+        sh.cval[i] = df_to_f(df_div(df_mul(sh.w[i], sh.rowZ[i]), sh.rowZ[N + i]));
+    }
+    // this stream's sweep claims: np items x ncl runs of kSegsPerClaim segments
+    const int ncl = (p.nseg + kSegsPerClaim - 1) / kSegsPerClaim;
+    if (tid == 0) {
+        sh.claim0 = np > 0 ? atomicAdd(&hdr->sweep_total, (unsigned long long)(np * ncl)) : 0ull;
+        // every stream appends at most (kmax + 1) ncl claims, so the list never overflows; the
+        // bound is kept anyway, and a stream that would cross it reports TIMEOUT
+        if (np > 0 && sh.claim0 + (unsigned long long)(np * ncl) > work_list_claims(p.B, p.kmax)) {
+            sh.status = SPEC_ST_TIMEOUT;
+            sh.n_pass = 0;
+        }
+    }
+    __syncthreads();
+
+    // ---- records for the sweep and finish kernels
+    const bool ok = sh.status == SPEC_ST_OK;
+    np = sh.n_pass;
+    if (ok) {
+        for (int r = (greedy ? N : 0) + tid; r < nrows; r += kThreads) {
+            RowStat* rs = blk_at<RowStat>(row_block(p, stats_row_of_part(gb, N, r)), kOffRow);
+            *rs = RowStat{sh.rowK[r], sh.rowZ[r].hi, sh.rowZ[r].lo, sh.rowArg[r]};
+        }
+        if (tid <= N) {
+            SlotRec* sr = blk_at<SlotRec>(row_block(p, gb + tid), kOffSlot);
+            const df qnan{__int_as_float(0x7fffffff), 0.f};
+            sr->rho = (!greedy && tid < N) ? sh.rho[tid] : qnan;
+            sr->w = sh.w[tid];
+            sr->h = qnan;
+            sr->r = qnan;
+            sr->cval = sh.cval[tid];
+            sr->x = tid < N ? sh.x[tid] : -1;
+            sr->lq = (!greedy && tid < N) ? sh.lq[tid] : 0.f;
+            sr->lp = (!greedy && tid < N) ? sh.lp[tid] : 0.f;
+        }
+        SweepItem* list = work_list(p);
+        for (int t = tid; t < np * ncl; t += kThreads) {
+            const int i = sh.pass_list[t / ncl];
+            const bool bonus = sh.bonus != 0;
+            list[sh.claim0 + t] = SweepItem{b,
+                                            (int16_t)i,
+                                            (int16_t)((t % ncl) * kSegsPerClaim),
+                                            bonus ? 0.f : sh.rowK[i],
+                                            sh.rowK[N + i],
+                                            bonus ? 1.f : sh.cval[i],
+                                            a.hi,
+                                            a.lo,
+                                            bonus ? 1 : 0};
+        }
+    }
+    if (tid == 0) {
+        StreamRec* srec = blk_at<StreamRec>(row_block(p, gb), kOffStream);
+        srec->status = sh.status;
+        srec->N = N;
+        srec->greedy = greedy ? 1 : 0;
+        srec->tau = sh.tau;
+        srec->n_pass = ok ? np : 0;
+        srec->bonus = sh.bonus;
+        srec->a_hi = a.hi;
+        srec->a_lo = a.lo;
+        for (int i = 0; i < np; ++i) srec->pass[i] = (uint8_t)sh.pass_list[i];
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// sweep_kernel: residual (or bonus) sums of every stream's sweep items, spread over the GPU
+// ---------------------------------------------------------------------------------------
+// A stage is G chunks of both rows of an item (q and p; p alone for the bonus row).  The
+// vector path (E = 8, 16-byte aligned rows) moves a stage with one TMA bulk copy per row into a
+// per-warp ring of D stages, each completing on its own mbarrier (lane 0 issues, every lane
+// waits with a bounded poll); the plain path (E = 1) loads chunk by chunk.
+template <typename DQ, typename DP, int E>
+struct SweepRing;
+
+template <typename DQ, typename DP>
+struct SweepRing<DQ, DP, 8> {
+    static constexpr int BQ = 8 * (int)sizeof(DQ);
+    static constexpr int BP = 8 * (int)sizeof(DP);
+    static constexpr int G = 2048 / (BQ > BP ? BQ : BP);   // chunks per stage and row
+    static constexpr int ROWQ = G * BQ;
+    static constexpr int STAGE = G * (BQ + BP);
+    static constexpr int D = 3;
+    static constexpr int RING = D * STAGE + 64;   // bytes per warp (stages + barriers)
+    char* base;
+    uint64_t* bar;
+    int lane;
+    unsigned phase;     // parity of the next completion of each slot
+    unsigned pending;   // slots with a stage issued and not yet waited for
+    bool timeout;
+    __device__ __forceinline__ void init(char* b, int ln) {
+        base = b;
+        bar = reinterpret_cast<uint64_t*>(b + D * STAGE);
+        lane = ln;
+        phase = 0;
+        pending = 0;
+        timeout = false;
+        if (lane == 0) {
+            for (int i = 0; i < D; ++i) mbar_init(&bar[i], 1);
+            mbar_init_fence();
+        }
+        __syncwarp();
+    }
+    // chunks [c0, c0 + n) of both rows into ring slot `slot` (rq null: p only)
+    __device__ __forceinline__ void issue(int slot, const void* rq, const void* rp, int64_t c0, int n) {
+        if (timeout || n <= 0) return;   // after a failed wait nothing new is put in flight
+        pending |= 1u << slot;
+        __syncwarp();                    // every lane is done reading this slot's previous stage
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_expect_tx(&bar[slot], (unsigned)(n * ((rq ? BQ : 0) + BP)));
+            if (rq)
+                bulk_g2s_hint(base + slot * STAGE, reinterpret_cast<const char*>(rq) + c0 * BQ, (unsigned)(n * BQ),
+                              &bar[slot], l2_evict_first_policy());
+            bulk_g2s_hint(base + slot * STAGE + ROWQ, reinterpret_cast<const char*>(rp) + c0 * BP, (unsigned)(n * BP),
+                          &bar[slot], l2_evict_first_policy());
+        }
+    }
+    __device__ __forceinline__ void wait(int slot, int n) {
+        if (timeout || n <= 0) return;
+        const unsigned parity = (phase >> slot) & 1u;
+        int k = 0;
+        while (!mbar_try_wait(&bar[slot], parity)) {
+            if (++k > kSpinLimit) {
+                timeout = true;   // the slot stays pending; drain() waits for it once more
+                return;
+            }
+        }
+        phase ^= 1u << slot;
+        pending &= ~(1u << slot);
+    }
+    // before the CTA exits: wait (bounded) for any copy still in flight after a failed wait
+    __device__ __forceinline__ void drain() {
+        for (int slot = 0; slot < D; ++slot) {
+            if (!((pending >> slot) & 1u)) continue;
+            const unsigned parity = (phase >> slot) & 1u;
+            for (int k = 0; k < kSpinLimit && !mbar_try_wait(&bar[slot], parity); ++k) {
+            }
+        }
+    }
+    __device__ __forceinline__ void get(int slot, int kk, const void*, const void*, int64_t, bool has_q,
+                                        float (&xq)[8], float (&xp)[8]) const {
+        if (has_q) unpack<DQ>(base + slot * STAGE + kk * BQ, xq);
+        unpack<DP>(base + slot * STAGE + ROWQ + kk * BP, xp);
+    }
+    template <typename T>
+    __device__ __forceinline__ static void unpack(const char* s, float (&x)[8]) {
+        if constexpr (sizeof(T) == 2) {
+            const uint4 v = *reinterpret_cast<const uint4*>(s);
+            x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+            x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+        } else {
+            const float4 a = *reinterpret_cast<const float4*>(s);
+            const float4 b = *reinterpret_cast<const float4*>(s + 16);
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+            x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        }
+    }
+};
+
+template <typename DQ, typename DP>
+struct SweepRing<DQ, DP, 1> {
+    static constexpr int G = 128;
+    static constexpr int D = 1;
+    static constexpr int RING = 0;
+    bool timeout;
+    __device__ __forceinline__ void init(char*, int) { timeout = false; }
+    __device__ __forceinline__ void issue(int, const void*, const void*, int64_t, int) {}
+    __device__ __forceinline__ void wait(int, int) {}
+    __device__ __forceinline__ void drain() {}
+    __device__ __forceinline__ void get(int, int kk, const void* rq, const void* rp, int64_t c0, bool has_q,
+                                        float (&xq)[1], float (&xp)[1]) const {
+        if (has_q) xq[0] = load_elem<DQ>(rq, c0 + kk);
+        xp[0] = load_elem<DP>(rp, c0 + kk);
+    }
+};
+
+// Sums of segments [s0, s1) of one item into seg_out[s0 .. s1): max(0, c 2^(lp a - Kp) -
+// 2^(lq a - Kq)) for a residual item, 2^(lp a - Kp) for the bonus row.  Stages never straddle
+// a segment; each segment's lane sums enter a Kahan sum stage by stage and are combined across
+// the warp in double-float.  after_last() runs in every lane right after the last copy.
+template <typename DQ, typename DP, int E, typename AfterFn>
+__device__ __forceinline__ void sweep_segments(SweepRing<DQ, DP, E>& R, const VerifyParams& p, const void* rq,
+                                               const void* rp, int s0, int s1, float Kq, float Kp, float ah,
+                                               float al, float cc, bool bonus, int lane, float* seg_out,
+                                               AfterFn after_last) {
+    using Ring = SweepRing<DQ, DP, E>;
+    constexpr int G = Ring::G, D = Ring::D;
+    const int64_t sc = p.seg_chunks;
+    const int mps = (int)((sc + G - 1) / G);   // stages per segment
+    const int nst = (s1 - s0) * mps;
+    auto stage = [&](int t, int64_t& c0, int& n) {
+        const int s = s0 + t / mps, m = t % mps;
+        const int64_t seg_end = min(p.nchunk, (int64_t)(s + 1) * sc);
+        c0 = (int64_t)s * sc + (int64_t)m * G;
+        const int64_t left = seg_end - c0;
+        n = left <= 0 ? 0 : (int)(left < G ? left : G);
+    };
+    const void* q = bonus ? nullptr : rq;
+    auto issue = [&](int t) {
+        if (t < nst) {
+            int64_t c0;
+            int n;
+            stage(t, c0, n);
+            R.issue(t % D, q, rp, c0, n);
+            if (t == nst - 1) after_last();
+        }
+    };
+    for (int t = 0; t < D - 1; ++t) issue(t);
+    Kahan acc;
+    for (int t = 0; t < nst; ++t) {
+        issue(t + D - 1);
+        int64_t c0;
+        int n;
+        stage(t, c0, n);
+        R.wait(t % D, n);
+        float grp = 0.f;   // this lane's chunk sums of the stage (independent), added once
+        for (int kk = lane; kk < n; kk += 32) {
+            float xq[E], xp[E];
+            R.get(t % D, kk, rq, rp, c0, !bonus, xq, xp);
+            grp += bonus ? target_chunk_sum<E>(xp, Kp, ah, al) : resid_chunk_sum<E>(xq, xp, Kq, Kp, ah, al, cc);
+        }
+        acc.add(grp);
+        if (t % mps == mps - 1) {   // the segment is complete
+            df tot = acc.value();
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const df other{__shfl_xor_sync(0xffffffffu, tot.hi, o), __shfl_xor_sync(0xffffffffu, tot.lo, o)};
+                tot = df_add(tot, other);
+            }
+            if (lane == 0) seg_out[s0 + t / mps] = df_to_f(tot);
+            acc = Kahan();
+        }
+    }
+    if (nst == 0) after_last();
+}
+
+template <typename DQ, typename DP, int E>
+__global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const VerifyParams p) {
+    extern __shared__ __align__(16) char ring_smem[];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    SweepRing<DQ, DP, E> ring;
+    ring.init(ring_smem + warp * SweepRing<DQ, DP, E>::RING, lane);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    WsHeader* hdr = ws_header(p);
+    const unsigned long long cap = work_list_claims(p.B, p.kmax);
+    const unsigned long long appended = __ldcg(&hdr->sweep_total);
+    const unsigned long long total = appended < cap ? appended : cap;
+    const SweepItem* list = work_list(p);
+    const int64_t V = p.V;
+    // a claim's entry: 32 bytes, lanes 0..7 hold one 32-bit word each
+    auto load_entry = [&](unsigned long long id) -> int {
+        return (lane < 8 && id < total) ? __ldcg(reinterpret_cast<const int*>(list + id) + lane) : 0;
+    };
+    // warp gw's first claim is gw itself; later claims come from the ticket, offset by the
+    // number of warps
+    const unsigned long long W = (unsigned long long)gridDim.x * kWarps;
+    unsigned long long claim = 0;
+    unsigned long long cur = (unsigned long long)blockIdx.x * kWarps + warp;
+    int word = load_entry(cur);
+    while (cur < total) {
+        const int b = __shfl_sync(0xffffffffu, word, 0);
+        const int w1 = __shfl_sync(0xffffffffu, word, 1);
+        const int i = (int)(int16_t)(w1 & 0xffff), s0 = (w1 >> 16) & 0xffff;
+        const float Kq = __int_as_float(__shfl_sync(0xffffffffu, word, 2));
+        const float Kp = __int_as_float(__shfl_sync(0xffffffffu, word, 3));
+        const float cc = __int_as_float(__shfl_sync(0xffffffffu, word, 4));
+        const float ah = __int_as_float(__shfl_sync(0xffffffffu, word, 5));
+        const float al = __int_as_float(__shfl_sync(0xffffffffu, word, 6));
+        const bool bonus = __shfl_sync(0xffffffffu, word, 7) != 0;
+        if (lane == 0) claim = W + atomicAdd(&hdr->ticket_sweep, 1ull);   // the next claim, in flight
+        unsigned long long nxt = total;
+        int nword = 0;
+        const int64_t gb = 2 * (int64_t)p.cu[b] + b;
+        const void* rq = bonus ? nullptr : row_ptr<DQ>(p.dq, (int64_t)p.cu[b] + i, V);
+        const void* rp = row_ptr<DP>(p.dp, (int64_t)p.cu[b] + b + i, V);
+        const int s1 = min(p.nseg, s0 + kSegsPerClaim);
+        // once this claim's last copy is issued: the next claim's entry is loaded while the
+        // rest of this one is summed
+        sweep_segments<DQ, DP, E>(ring, p, rq, rp, s0, s1, Kq, Kp, ah, al, cc, bonus, lane,
+                                  blk_at<float>(row_block(p, gb + i), kOffSeg), [&]() {
+                                      nxt = __shfl_sync(0xffffffffu, claim, 0);
+                                      nword = load_entry(nxt);
+                                  });
+        if (lane == 0) {
+            char* sblk = row_block(p, gb);
+            if (ring.timeout) atomicExch(blk_at<unsigned>(sblk, kOffSweepTimeout), 1u);
+            atomicAdd(blk_at<unsigned>(sblk, kOffSweepCount), (unsigned)(s1 - s0));
+        }
+        cur = nxt;
+        word = nword;
+    }
+    // no TMA copy of this warp may still be writing its ring when the CTA leaves
+    ring.drain();
+}
+
+// ---------------------------------------------------------------------------------------
+// finish_kernel: one CTA per stream - r_i, h_i, tau, the draw, the outputs
+// ---------------------------------------------------------------------------------------
+struct FinishShared {
+    float rowK[kMaxRows];
+    df rowZ[kMaxRows];
+    int rowArg[kMaxRows];
+    df rho[SPEC_MAX_KMAX];
+    df w[SPEC_MAX_KMAX + 1];
+    df h[SPEC_MAX_KMAX + 1];
+    df r[SPEC_MAX_KMAX + 1];
+    df u_acc[SPEC_MAX_KMAX + 1];
+    uint32_t u_smp[SPEC_MAX_KMAX + 1];
+    float cval[SPEC_MAX_KMAX + 1];
+    float lq[SPEC_MAX_KMAX], lp[SPEC_MAX_KMAX];
+    int x[SPEC_MAX_KMAX];
+    int pass_list[SPEC_MAX_KMAX + 1];
+    int N, n_pass, status, greedy, tau, bonus, sample_seg;
+    unsigned long long sample_t;                 // in-segment target (fixed point)
+    unsigned long long sub_sum[kWarps];          // the drawn segment split over the warps
+    int sub_last[kWarps];
+    float sample_scale;                          // fixed-point scale of the draw's weights
+    float a_hi, a_lo;
+    unsigned sweep_count, sweep_timeout;
+    float seg[SPEC_MAX_KMAX + 1][kSegs];         // every slot's segment sums (swept slots hold data)
+};
+
+template <typename DQ, typename DP, int E>
+__global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) {
+    __shared__ FinishShared sh;
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t V = p.V;
+    const int64_t ob = (int64_t)b * (p.kmax + 1);
+    // ---- prologue (inputs only): the per-slot uniforms and the stream's offsets
+    if (tid <= p.kmax) {
+        const uint4 c = make_uint4((uint32_t)tid, (uint32_t)b, (uint32_t)p.step, (uint32_t)(p.step >> 32));
+        const uint4 wds = philox4x32_10(c, make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
+        sh.u_acc[tid] = uniform24_df(wds.x);
+        sh.u_smp[tid] = wds.y;
+        sh.h[tid] = df{__int_as_float(0x7fffffff), 0.f};
+        sh.r[tid] = df{__int_as_float(0x7fffffff), 0.f};
+    }
+    const int base = p.cu[b];
+    const int n_raw = p.cu[b + 1] - base;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    WsHeader* hdr = ws_header(p);
+    if (b == 0 && tid == 0) {   // the sweep grid has finished: its ticket and list go back to zero
+        hdr->ticket_sweep = 0ull;
+        hdr->sweep_total = 0ull;
+    }
+    const int L = __ldcg(&hdr->L);
+    if (b >= L) {
+        for (int j = tid; j <= p.kmax; j += kThreads) p.out_tok[ob + j] = -1;
+        if (tid == 0) {
+            p.status[b] = SPEC_ST_BAD_OFFSETS;
+            p.acc_len[b] = 0;
+            p.n_emit[b] = 0;
+        }
+        return;
+    }
+    const int N = n_raw;
+    const int64_t gb = 2 * (int64_t)base + b;
+    const int nrows = 2 * N + 1;
+    char* sblk = row_block(p, gb);
+    // ---- one round of loads: the stream's record, every row's statistics, every slot's
+    // scalars and segment sums (decide_kernel wrote the records of every OK stream; the
+    // segment sums of slots that were not swept are not used)
+    if (tid == 0) {
+        const StreamRec* sr = blk_at<StreamRec>(sblk, kOffStream);
+        sh.status = __ldcg(&sr->status);
+        sh.N = N;
+        sh.greedy = __ldcg(&sr->greedy);
+        sh.tau = __ldcg(&sr->tau);
+        sh.n_pass = __ldcg(&sr->n_pass);
+        sh.bonus = __ldcg(&sr->bonus);
+        sh.a_hi = __ldcg(&sr->a_hi);
+        sh.a_lo = __ldcg(&sr->a_lo);
+        const int4 pl[3] = {__ldcg(reinterpret_cast<const int4*>(sr->pass)),
+                            __ldcg(reinterpret_cast<const int4*>(sr->pass) + 1),
+                            __ldcg(reinterpret_cast<const int4*>(sr->pass) + 2)};
+        const unsigned char* pb = reinterpret_cast<const unsigned char*>(pl);
+        for (int i = 0; i <= SPEC_MAX_KMAX; ++i) sh.pass_list[i] = pb[i];
+        sh.sweep_count = __ldcg(blk_at<unsigned>(sblk, kOffSweepCount));
+        sh.sweep_timeout = __ldcg(blk_at<unsigned>(sblk, kOffSweepTimeout));
+        sh.sample_seg = -1;
+    }
+    for (int r = tid; r < nrows; r += kThreads) {
+        const RowStat* rs = blk_at<RowStat>(row_block(p, stats_row_of_part(gb, N, r)), kOffRow);
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(rs));
+        sh.rowK[r] = v.x;
+        sh.rowZ[r] = df{v.y, v.z};
+        sh.rowArg[r] = __float_as_int(v.w);
+    }
+    if (tid <= N) {
+        const SlotRec* sr = blk_at<SlotRec>(row_block(p, gb + tid), kOffSlot);
+        if (tid < N) {
+            sh.rho[tid] = df{__ldcg(&sr->rho.hi), __ldcg(&sr->rho.lo)};
+            sh.x[tid] = __ldcg(&sr->x);
+            sh.lq[tid] = __ldcg(&sr->lq);
+            sh.lp[tid] = __ldcg(&sr->lp);
+        }
+        sh.w[tid] = df{__ldcg(&sr->w.hi), __ldcg(&sr->w.lo)};
+        sh.cval[tid] = __ldcg(&sr->cval);
+    }
+    for (int t = tid; t < (N + 1) * p.nseg; t += kThreads) {
+        const int i = t / p.nseg, sg = t - i * p.nseg;
+        sh.seg[i][sg] = __ldcg(blk_at<const float>(row_block(p, gb + i), kOffSeg) + sg);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        if (sh.status == SPEC_ST_OK && !sh.greedy && sh.n_pass > 0) {
+            if (sh.sweep_timeout != 0u || sh.sweep_count != (unsigned)(sh.n_pass * p.nseg))
+                sh.status = SPEC_ST_TIMEOUT;
+            *blk_at<unsigned>(sblk, kOffSweepCount) = 0u;   // back to zero for the next call
+            *blk_at<unsigned>(sblk, kOffSweepTimeout) = 0u;
+        }
+    }
+    __syncthreads();
+    const bool greedy = sh.greedy != 0;
+    const float ah = sh.a_hi, al = sh.a_lo;
+    const df one{1.f, 0.f};
+    const bool block = (p.rule == 1);
+    auto qrow = [&](int i) { return row_ptr<DQ>(p.dq, (int64_t)base + i, V); };
+    auto prow = [&](int i) { return row_ptr<DP>(p.dp, (int64_t)base + b + i, V); };
+
+    if (sh.status == SPEC_ST_OK && !greedy && sh.n_pass > 0) {
+        const int np = sh.n_pass;
+        const bool bonus_sweep = sh.bonus != 0;
+        // ---- r_i = (sum of the item's segment sums) / Z_q, per item (same order every time)
+        for (int it = warp; it < np && !bonus_sweep; it += kWarps) {
+            const int i = sh.pass_list[it];
+            df tot{0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int sg = lane + 32 * k;
+                tot = df_add_f(tot, sg < p.nseg ? sh.seg[i][sg] : 0.f);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const df other{__shfl_xor_sync(0xffffffffu, tot.hi, o), __shfl_xor_sync(0xffffffffu, tot.lo, o)};
+                tot = df_add(tot, other);
+            }
+            if (lane == 0) {
+                const df ri = df_div(tot, sh.rowZ[i]);
+                sh.r[i] = ri;
+                if (block && i >= 1) {
+                    const df den = df_add(ri, df_sub(one, sh.w[i]));
+                    sh.h[i] = df_is_zero(den) ? one : df_div(ri, den);
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == 0 && block && !bonus_sweep) {
+            int tau = 0;
+            for (int it = 0; it < np; ++it) {   // candidates in descending order, then slot 0
+                const int i = sh.pass_list[it];
+                if (i >= 1 && df_le(sh.u_acc[i - 1], sh.h[i])) {
+                    tau = i;
+                    break;
+                }
+            }
             sh.tau = tau;
         }
         __syncthreads();
-    } else if (sh.status == SPEC_ST_OK) {
-        const bool block = (p.rule == 1);
-        if (tid == 0) {
-            int n = 0;
-            if (block) {
-                sh.w[0] = one;
-                for (int i = 0; i < N; ++i) sh.w[i + 1] = df_min(one, df_mul(sh.w[i], sh.rho[i]));
-                sh.tau = 0;
-                if (N > 0) sh.h[N] = sh.w[N];
-                if (N > 0 && df_le(sh.u_acc[N - 1], sh.h[N])) {
-                    sh.tau = N;   // eta_N <= w_N: accept everything, no residual needed
-                } else {
-                    for (int i = N - 1; i >= 1; --i)   // candidates: eta_i <= w_i (h_i <= w_i)
-                        if (df_le(sh.u_acc[i - 1], sh.w[i])) sh.pass_list[n++] = i;
-                    if (N > 0) sh.pass_list[n++] = 0;
-                }
-            } else {
-                int tau = N;
-                for (int i = 0; i < N; ++i)
-                    if (!df_le(sh.u_acc[i], df_min(one, sh.rho[i]))) {
-                        tau = i;
-                        break;
-                    }
-                sh.tau = tau;
-                if (tau < N) {
-                    sh.w[tau] = one;
-                    sh.pass_list[n++] = tau;
-                }
-            }
-            if (sh.tau == N) {   // every draft accepted: the sweep sums the bonus row instead
-                sh.pass_list[0] = N;
-                n = 1;
-                sh.sample_bonus = 1;
-            }
-            sh.n_pass = n;
-        }
-        __syncthreads();
-        np = sh.n_pass;
-        const bool bonus_sweep = sh.sample_bonus != 0;
-        if (tid < np && !bonus_sweep) {
-            const int i = sh.pass_list[tid];
-            sh.cval[i] = df_to_f(df_div(df_mul(sh.w[i], sh.rowZ[i]), sh.rowZ[N + i]));
-        }
-        __syncthreads();
 
-        // ---- one cluster-wide residual sweep over every slot that may be needed
-        if (np > 0) {
-            Kahan acc;
-            float grp = 0.f;   // this lane's chunk sums of the current group (independent), added once
-            float Kq = 0.f, Kp = 0.f, cc = 0.f;
-            sweep<DQ, DP, E>(
-                feed, np, c0, c1, lane,
-                [&](int it, const void*& rq, const void*& rp) {
-                    const int i = sh.pass_list[it];
-                    rq = bonus_sweep ? nullptr : qrow(i);
-                    rp = prow(i);
-                },
-                [&](int it) {
-                    const int i = sh.pass_list[it];
-                    Kq = bonus_sweep ? 0.f : sh.rowK[i];
-                    Kp = sh.rowK[N + i];
-                    cc = bonus_sweep ? 1.f : sh.cval[i];
-                    acc = Kahan();
-                },
-                [&](int64_t, const float (&xq)[E], const float (&xp)[E]) {
-                    if (bonus_sweep) grp += target_chunk_sum<E>(xp, Kp, ah, al);
-                    else grp += resid_chunk_sum<E>(xq, xp, Kq, Kp, ah, al, cc);
-                },
-                [&](int it) {
-                    df tot = acc.value();
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const df other{__shfl_xor_sync(0xffffffffu, tot.hi, o), __shfl_xor_sync(0xffffffffu, tot.lo, o)};
-                        tot = df_add(tot, other);
-                    }
-                    if (lane == 0) sh.res_part[it][warp] = df_to_f(tot);
-                },
-                [&]() {
-                    acc.add(grp);
-                    grp = 0.f;
-                });
-            if (lane == 0 && feed.timeout) sh.to_flag[warp] = 1;
-        }
-    }
-
-    // ---- every CTA of the cluster meets here exactly once, whatever its status, so the CTAs
-    // cannot part ways at a cluster barrier; a bounded wait that gave up in any of them (their
-    // statuses may differ only there) makes the stream TIMEOUT in all of them
-    cluster_sync_all();
-    {
-        bool to = false;
-        if (tid < nseg) to = *cluster.map_shared_rank(&sh.to_flag[tid % kWarps], tid / kWarps) != 0;
-        to = __syncthreads_or(to);
-        if (to && tid == 0 && sh.status == SPEC_ST_OK) sh.status = SPEC_ST_TIMEOUT;
-        __syncthreads();
-    }
-
-    if (sh.status == SPEC_ST_OK && !greedy) {
-        const bool block = (p.rule == 1);
-        const bool bonus_sweep = sh.sample_bonus != 0;
-        np = sh.n_pass;
-        if (np > 0) {
-            // per pass item: r_i = (sum over all segments) / Z_q
-            for (int it = warp; it < np && !bonus_sweep; it += kWarps) {
-                df tot{0.f, 0.f};
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int s = lane + 32 * k;
-                    const float v = (s < nseg) ? *cluster.map_shared_rank(&sh.res_part[it][s % kWarps], s / kWarps) : 0.f;
-                    tot = df_add_f(tot, v);
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const df other{__shfl_xor_sync(0xffffffffu, tot.hi, o), __shfl_xor_sync(0xffffffffu, tot.lo, o)};
-                    tot = df_add(tot, other);
-                }
-                if (lane == 0) {
-                    const int i = sh.pass_list[it];
-                    const df ri = df_div(tot, sh.rowZ[i]);
-                    sh.r[i] = ri;
-                    if (block && i >= 1) {
-                        const df den = df_add(ri, df_sub(one, sh.w[i]));
-                        sh.h[i] = df_is_zero(den) ? one : df_div(ri, den);
-                    }
-                }
-            }
-            __syncthreads();
-            if (tid == 0 && block) {
-                int tau = 0;
-                for (int it = 0; it < np; ++it) {   // candidates in descending order, then slot 0
-                    const int i = sh.pass_list[it];
-                    if (i >= 1 && df_le(sh.u_acc[i - 1], sh.h[i])) {
-                        tau = i;
-                        break;
-                    }
-                }
-                sh.tau = tau;
-            }
-            __syncthreads();
-        }
-
-        // ---- the draw: 64-bit fixed-point CDF over the segments (warp 0)
+        // ---- the draw: 64-bit fixed-point CDF over the drawn item's segments (warp 0)
         if (warp == 0) {
             const int tau = sh.tau;
-            const bool bonus = (tau == N);
-            int item = 0;
-            for (int it = 0; it < np; ++it)
-                if (sh.pass_list[it] == tau) item = it;
-            float w0 = 0.f, w1 = 0.f;
-            if (lane < nseg) w0 = *cluster.map_shared_rank(&sh.res_part[item][lane % kWarps], lane / kWarps);
-            if (lane + 32 < nseg)
-                w1 = *cluster.map_shared_rank(&sh.res_part[item][(lane + 32) % kWarps], (lane + 32) / kWarps);
+            const float w0 = lane < p.nseg ? sh.seg[tau][lane] : 0.f;
+            const float w1 = lane + 32 < p.nseg ? sh.seg[tau][lane + 32] : 0.f;
             const float wmax = warp_max(fmaxf(w0, w1));
             const bool ok = isfinite(wmax) && wmax > 0.f;
             const float scale = ok ? fixed_scale(wmax) : 0.f;
@@ -1483,19 +1559,18 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
             const unsigned long long t = (__umul64hi(odd, R) << 39) | ((odd * R) >> 25);
             const unsigned h0 = __ballot_sync(0xffffffffu, q0 > 0 && p0 > t);
             const unsigned h1 = __ballot_sync(0xffffffffu, q1 > 0 && p1 > t);
-            const int seg = h0 ? __ffs(h0) - 1 : (h1 ? 32 + __ffs(h1) - 1 : -1);
-            const int src = seg < 0 ? 0 : seg % 32;
+            const int sg = h0 ? __ffs(h0) - 1 : (h1 ? 32 + __ffs(h1) - 1 : -1);
+            const int src = sg < 0 ? 0 : sg % 32;
             const unsigned long long i0 = __shfl_sync(0xffffffffu, p0, src);
             const unsigned long long i1 = __shfl_sync(0xffffffffu, p1, src);
             const unsigned long long qs0 = __shfl_sync(0xffffffffu, q0, src);
             const unsigned long long qs1 = __shfl_sync(0xffffffffu, q1, src);
             if (lane == 0) {
-                if (ok && R > 0 && seg >= 0) {
-                    const unsigned long long excl = (seg < 32) ? i0 - qs0 : i1 - qs1;
+                if (ok && R > 0 && sg >= 0) {
+                    const unsigned long long excl = (sg < 32) ? i0 - qs0 : i1 - qs1;
                     sh.sample_t = t - excl;
                     sh.sample_scale = scale;
-                    sh.sample_seg = seg;
-                    sh.sample_bonus = bonus;
+                    sh.sample_seg = sg;
                 } else {
                     sh.status = SPEC_ST_NUMERIC;
                     sh.sample_seg = -1;
@@ -1503,116 +1578,104 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
             }
         }
         __syncthreads();
-    }
 
-    // every distributed-shared-memory read of this CTA is done: arrive now, wait at the end
-    cluster_arrive();
-
-    // ---- the rescan of the drawn segment, split over the warps of the CTA that owns it: each
-    // warp sums an eighth in fixed point, the eighth that crosses the target is rescanned
-    if (sh.status == SPEC_ST_OK && !greedy && sh.sample_seg >= 0 && crank == sh.sample_seg / kWarps) {
-        const int tau = sh.tau;
-        const bool bonus = sh.sample_bonus != 0;
-        const void* rq = bonus ? nullptr : qrow(tau);
-        const void* rp = bonus ? prow(N) : prow(tau);
-        const float Kq = bonus ? 0.f : sh.rowK[tau], Kp = bonus ? sh.rowK[2 * N] : sh.rowK[N + tau];
-        const float cc = bonus ? 0.f : sh.cval[tau];
-        const int64_t s0 = min(p.nchunk, (int64_t)sh.sample_seg * p.seg_chunks);
-        const int64_t s1 = min(p.nchunk, s0 + p.seg_chunks);
-        const int64_t msub = (s1 - s0 + kWarps - 1) / kWarps;
-        const int64_t w0 = min(s1, s0 + warp * msub), w1 = min(s1, w0 + msub);
-        unsigned long long sub;
-        int last;
-        if (bonus)
-            segment_fixed_sum<DQ, DP, E, true>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, lane, sub, last);
-        else
-            segment_fixed_sum<DQ, DP, E, false>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, lane, sub, last);
-        if (lane == 0) {
-            sh.sub_sum[warp] = sub;
-            sh.sub_last[warp] = last;
-        }
-        __syncthreads();
-        const unsigned long long t = sh.sample_t;
-        unsigned long long before = 0;
-        int wsel = -1, lastpos = -1;
-        for (int w = 0; w < kWarps; ++w) {
-            lastpos = max(lastpos, sh.sub_last[w]);
-            if (wsel < 0) {
-                if (sh.sub_sum[w] > 0 && before + sh.sub_sum[w] > t) wsel = w;
-                else before += sh.sub_sum[w];
+        // ---- the rescan of the drawn segment, split over the warps: each warp sums an eighth in
+        // fixed point, the eighth that crosses the target is rescanned
+        if (sh.status == SPEC_ST_OK && sh.sample_seg >= 0) {
+            const int tau = sh.tau;
+            const bool bonus = (tau == N);
+            const void* rq = bonus ? nullptr : qrow(tau);
+            const void* rp = prow(tau);
+            const float Kq = bonus ? 0.f : sh.rowK[tau], Kp = sh.rowK[N + tau];
+            const float cc = bonus ? 0.f : sh.cval[tau];
+            const int64_t s0 = min(p.nchunk, (int64_t)sh.sample_seg * p.seg_chunks);
+            const int64_t s1 = min(p.nchunk, s0 + p.seg_chunks);
+            const int64_t msub = (s1 - s0 + kWarps - 1) / kWarps;
+            const int64_t w0 = min(s1, s0 + warp * msub), w1 = min(s1, w0 + msub);
+            unsigned long long sub;
+            int last;
+            if (bonus)
+                segment_fixed_sum<DQ, DP, E, true>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, lane, sub,
+                                                   last);
+            else
+                segment_fixed_sum<DQ, DP, E, false>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, lane, sub,
+                                                    last);
+            if (lane == 0) {
+                sh.sub_sum[warp] = sub;
+                sh.sub_last[warp] = last;
             }
-        }
-        int y = -1;
-        if (wsel < 0) {
-            y = lastpos;   // rounding kept the segment's sum at or below the target
-        } else if (warp == wsel) {
-            y = bonus ? rescan_segment<DQ, DP, E, true>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, t - before, lane)
-                      : rescan_segment<DQ, DP, E, false>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, t - before,
-                                                         lane);
-        }
-        if ((wsel < 0 && tid == 0) || (warp == wsel && lane == 0)) p.out_tok[(int64_t)b * (p.kmax + 1) + tau] = y;
-    }
-
-    // ---- outputs (CTA rank 0)
-    if (crank == 0) {
-        const int st = sh.status;
-        const int tau = sh.tau;
-        const int64_t ob = (int64_t)b * (p.kmax + 1);
-        for (int j = tid; j <= p.kmax; j += kThreads) {
-            if (st != SPEC_ST_OK) p.out_tok[ob + j] = -1;
-            else if (j < tau) p.out_tok[ob + j] = sh.x[j];
-            else if (j > tau) p.out_tok[ob + j] = -1;
-            else if (sh.greedy) p.out_tok[ob + j] = sh.rowArg[N + tau];
-        }
-        if (tid == 0) {
-            p.status[b] = st;
-            p.acc_len[b] = (st == SPEC_ST_OK) ? tau : 0;
-            p.n_emit[b] = (st == SPEC_ST_OK) ? tau + 1 : 0;
-        }
-        if (p.diag != nullptr && st != SPEC_ST_BAD_OFFSETS) {
-            const float qnan = __int_as_float(0x7fffffff);
-            const float ln2 = 0.6931471805599453f;
-            const bool have = (!sh.greedy) && (st == SPEC_ST_OK || st == SPEC_ST_NUMERIC);
-            for (int i = tid; i <= N; i += kThreads) {
-                float* d = p.diag + (tbase + i) * SPEC_DIAG_COLS;
-                float v[SPEC_DIAG_COLS];
-#pragma unroll
-                for (int c = 0; c < SPEC_DIAG_COLS; ++c) v[c] = qnan;
-                if (have) {
-                    // natural log of sum exp(l / T) = ln 2 (K + log2 Z)
-                    const df zp = sh.rowZ[N + i];
-                    v[SPEC_DIAG_LOGZP] = ln2 * (sh.rowK[N + i] + log2f(zp.hi)) + zp.lo / zp.hi;
-                    if (i < N) {
-                        const df zq = sh.rowZ[i];
-                        const float lq = sh.lq[i], lp = sh.lp[i];
-                        v[SPEC_DIAG_PX] =
-                            isfinite(lp) ? df_to_f(df_div(df_exp2(exponent_df(lp, ah, al, sh.rowK[N + i])), zp)) : 0.f;
-                        v[SPEC_DIAG_QX] =
-                            isfinite(lq) ? df_to_f(df_div(df_exp2(exponent_df(lq, ah, al, sh.rowK[i])), zq)) : 0.f;
-                        v[SPEC_DIAG_RHO] = df_to_f(sh.rho[i]);
-                        v[SPEC_DIAG_LOGZQ] = ln2 * (sh.rowK[i] + log2f(zq.hi)) + zq.lo / zq.hi;
-                    }
-                    if (p.rule == 1) {
-                        v[SPEC_DIAG_W] = df_to_f(sh.w[i]);
-                        if (i >= 1) v[SPEC_DIAG_H] = df_to_f(sh.h[i]);
-                    }
-                    v[SPEC_DIAG_R] = df_to_f(sh.r[i]);
+            __syncthreads();
+            const unsigned long long t = sh.sample_t;
+            unsigned long long before = 0;
+            int wsel = -1, lastpos = -1;
+            for (int w = 0; w < kWarps; ++w) {
+                lastpos = max(lastpos, sh.sub_last[w]);
+                if (wsel < 0) {
+                    if (sh.sub_sum[w] > 0 && before + sh.sub_sum[w] > t) wsel = w;
+                    else before += sh.sub_sum[w];
                 }
-#pragma unroll
-                for (int c = 0; c < SPEC_DIAG_COLS; ++c) d[c] = v[c];
             }
+            int y = -1;
+            if (wsel < 0) {
+                y = lastpos;   // rounding kept the segment's sum at or below the target
+            } else if (warp == wsel) {
+                y = bonus ? rescan_segment<DQ, DP, E, true>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale,
+                                                            t - before, lane)
+                          : rescan_segment<DQ, DP, E, false>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale,
+                                                             t - before, lane);
+            }
+            if ((wsel < 0 && tid == 0) || (warp == wsel && lane == 0)) p.out_tok[ob + tau] = y;
         }
     }
-    // no TMA copy of this warp may still be writing its ring when the CTA leaves
-    feed.drain();
-    // no CTA may leave while another can still read its shared memory
-    cluster_wait();
-    // The grid completes only after the stats grid (a stream with no rows, or whose wait gave
-    // up, never waited for it).  Then every stats add has landed and every CTA of the cluster
-    // has read its partials: the row counters go back to zero for the next call.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (crank == 0 && rows_written)
-        for (int r = (greedy ? N : 0) + tid; r < nrows; r += kThreads) *row_counter(p, stats_row(r)) = 0u;
+
+    // ---- outputs
+    const int st = sh.status;
+    const int tau = sh.tau;
+    for (int j = tid; j <= p.kmax; j += kThreads) {
+        if (st != SPEC_ST_OK) p.out_tok[ob + j] = -1;
+        else if (j < tau) p.out_tok[ob + j] = sh.x[j];
+        else if (j > tau) p.out_tok[ob + j] = -1;
+        else if (greedy) p.out_tok[ob + j] = sh.rowArg[N + tau];
+    }
+    if (tid == 0) {
+        p.status[b] = st;
+        p.acc_len[b] = (st == SPEC_ST_OK) ? tau : 0;
+        p.n_emit[b] = (st == SPEC_ST_OK) ? tau + 1 : 0;
+    }
+    if (p.diag != nullptr) {
+        const float qnan = __int_as_float(0x7fffffff);
+        const float ln2 = 0.6931471805599453f;
+        const bool have = (!greedy) && (st == SPEC_ST_OK || st == SPEC_ST_NUMERIC);
+        const int64_t tbase = (int64_t)base + b;
+        for (int i = tid; i <= N; i += kThreads) {
+            float* d = p.diag + (tbase + i) * SPEC_DIAG_COLS;
+            float v[SPEC_DIAG_COLS];
+#pragma unroll
+            for (int c = 0; c < SPEC_DIAG_COLS; ++c) v[c] = qnan;
+            if (have) {
+                // natural log of sum exp(l / T) = ln 2 (K + log2 Z)
+                const df zp = sh.rowZ[N + i];
+                v[SPEC_DIAG_LOGZP] = ln2 * (sh.rowK[N + i] + log2f(zp.hi)) + zp.lo / zp.hi;
+                if (i < N) {
+                    const df zq = sh.rowZ[i];
+                    const float lq = sh.lq[i], lp = sh.lp[i];
+                    v[SPEC_DIAG_PX] =
+                        isfinite(lp) ? df_to_f(df_div(df_exp2(exponent_df(lp, ah, al, sh.rowK[N + i])), zp)) : 0.f;
+                    v[SPEC_DIAG_QX] =
+                        isfinite(lq) ? df_to_f(df_div(df_exp2(exponent_df(lq, ah, al, sh.rowK[i])), zq)) : 0.f;
+                    v[SPEC_DIAG_RHO] = df_to_f(sh.rho[i]);
+                    v[SPEC_DIAG_LOGZQ] = ln2 * (sh.rowK[i] + log2f(zq.hi)) + zq.lo / zq.hi;
+                }
+                if (block) {
+                    v[SPEC_DIAG_W] = df_to_f(sh.w[i]);
+                    if (i >= 1) v[SPEC_DIAG_H] = df_to_f(i == N ? sh.w[N] : sh.h[i]);
+                }
+                v[SPEC_DIAG_R] = df_to_f(sh.r[i]);
+            }
+#pragma unroll
+            for (int c = 0; c < SPEC_DIAG_COLS; ++c) d[c] = v[c];
+        }
+    }
 }
 
 // Uniforms exposed for checking: out[(s * n_slots + i) * 2 + {0, 1}] (exact in double)
@@ -1631,127 +1694,95 @@ __global__ void philox_uniforms_kernel(uint64_t seed, uint64_t step, int n_strea
 // Host side
 // ---------------------------------------------------------------------------------------
 template <typename DQ, typename DP, int E>
-static size_t ring_bytes() {
-    return (size_t)kWarps * Feed<DQ, DP, E>::RING;
+static size_t sweep_smem_bytes() {
+    return (size_t)kWarps * SweepRing<DQ, DP, E>::RING;
 }
 
+static int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    return dev;
+}
+
+// Per kernel instantiation and device, set once: the dynamic shared memory limits and the two
+// persistent grid sizes (every SM filled to its occupancy).
 template <typename DQ, typename DP, int E>
-static cudaLaunchConfig_t make_config(int grid, int C, cudaStream_t s, cudaLaunchAttribute* attr) {
+struct LaunchCache {
+    static std::atomic<int> stats_grid[64];
+    static std::atomic<int> sweep_grid[64];
+};
+template <typename DQ, typename DP, int E>
+std::atomic<int> LaunchCache<DQ, DP, E>::stats_grid[64];
+template <typename DQ, typename DP, int E>
+std::atomic<int> LaunchCache<DQ, DP, E>::sweep_grid[64];
+
+template <typename DQ, typename DP, int E>
+static cudaError_t prepare(int* stats_grid, int* sweep_grid) {
+    using C = LaunchCache<DQ, DP, E>;
+    const int dev = current_device();
+    int g1 = C::stats_grid[dev].load(std::memory_order_acquire);
+    int g3 = C::sweep_grid[dev].load(std::memory_order_acquire);
+    if (g1 == 0 || g3 == 0) {
+        cudaError_t e = cudaFuncSetAttribute(stats_kernel<DQ, DP, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)stats_smem_bytes(E));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(sweep_kernel<DQ, DP, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)sweep_smem_bytes<DQ, DP, E>());
+        if (e != cudaSuccess) return e;
+        int sms = 0, occ1 = 0, occ3 = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, stats_kernel<DQ, DP, E>, kStatsThreads,
+                                                          stats_smem_bytes(E)) != cudaSuccess || occ1 < 1)
+            occ1 = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ3, sweep_kernel<DQ, DP, E>, kThreads,
+                                                          sweep_smem_bytes<DQ, DP, E>()) != cudaSuccess || occ3 < 1)
+            occ3 = 1;
+        cudaGetLastError();
+        g1 = sms * occ1;
+        g3 = sms * occ3;
+        C::stats_grid[dev].store(g1, std::memory_order_release);
+        C::sweep_grid[dev].store(g3, std::memory_order_release);
+    }
+    *stats_grid = g1;
+    *sweep_grid = g3;
+    return cudaSuccess;
+}
+
+// A launch that may begin while the previous kernel on the stream is still running (its
+// griddepcontrol.wait orders the data).
+template <typename Kernel>
+static cudaError_t launch_dependent(Kernel kernel, int grid, size_t smem, cudaStream_t s, const VerifyParams& p) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = ring_bytes<DQ, DP, E>();
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cfg;
-}
-
-template <typename DQ, typename DP, int E>
-static cudaError_t prepare_kernel() {
-    static int done[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    if (done[dev]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel<DQ, DP, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)ring_bytes<DQ, DP, E>());
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(stats_kernel<DQ, DP, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)stats_smem_bytes(E));
-    if (e == cudaSuccess) done[dev] = 1;
-    return e;
-}
-
-// How many clusters of C CTAs fit on the device at once (queried once per kernel, C, device).
-template <typename DQ, typename DP, int E>
-static int resident_clusters(int C) {
-    static int cache[kMaxCluster + 1][64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    int& slot = cache[C][dev];
-    if (slot == 0) {
-        cudaLaunchAttribute attr[1];
-        cudaLaunchConfig_t cfg = make_config<DQ, DP, E>(C, C, nullptr, attr);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, verify_kernel<DQ, DP, E>, &cfg) != cudaSuccess || n < 1) {
-            cudaGetLastError();
-            n = 1;
-        }
-        slot = n;
-    }
-    return slot;
-}
-
-// Cluster size: each stream is one cluster; a larger cluster finishes its stream sooner, but
-// streams beyond the resident cluster count run in extra waves.  Minimise waves / C, with at
-// least 64 chunks per warp segment (small vocabularies use small clusters).
-template <typename DQ, typename DP, int E>
-static int pick_cluster(int B, int64_t nchunk) {
-    int cmax = (int)(nchunk / (kWarps * 64));
-    cmax = cmax < 1 ? 1 : (cmax > kMaxCluster ? kMaxCluster : cmax);
-    int best = 1;
-    double best_cost = 1e300;
-    for (int C = 1; C <= cmax; ++C) {
-        const int res = resident_clusters<DQ, DP, E>(C);
-        const double waves = (double)((B + res - 1) / res);
-        const double cost = waves / C;
-        if (cost < best_cost * (1.0 - 1e-9)) {
-            best_cost = cost;
-            best = C;
-        }
-    }
-    return best;
-}
-
-// Persistent grid of the stats kernel: every SM filled to its occupancy.
-template <typename DQ, typename DP, int E>
-static int stats_grid() {
-    static int cache[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    if (cache[dev] == 0) {
-        int sms = 0, occ = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, stats_kernel<DQ, DP, E>, kThreads,
-                                                          stats_smem_bytes(E)) != cudaSuccess ||
-            occ < 1) {
-            cudaGetLastError();
-            occ = 1;
-        }
-        cache[dev] = sms * occ;
-    }
-    return cache[dev];
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 template <typename DQ, typename DP, int E>
 static cudaError_t run_verify(VerifyParams& p, cudaStream_t s, int* info) {
-    cudaError_t e = prepare_kernel<DQ, DP, E>();
+    int g1 = 0, g3 = 0;
+    cudaError_t e = prepare<DQ, DP, E>(&g1, &g3);
     if (e != cudaSuccess) return e;
-    const int C = pick_cluster<DQ, DP, E>(p.B, p.nchunk);
-    p.seg_chunks = (p.nchunk + (int64_t)C * kWarps - 1) / ((int64_t)C * kWarps);
     if (info) {
-        info[0] = C;
-        info[1] = resident_clusters<DQ, DP, E>(C);
+        info[0] = 1;
+        info[1] = g3;
         return cudaSuccess;
     }
-    const int grid = stats_grid<DQ, DP, E>();
-    p.stats_warps = (int64_t)grid * kWarps;
-    stats_kernel<DQ, DP, E><<<grid, kThreads, stats_smem_bytes(E), s>>>(p);
+    p.stats_warps = (int64_t)g1 * kStatsWarps;
+    stats_kernel<DQ, DP, E><<<g1, kStatsThreads, stats_smem_bytes(E), s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = make_config<DQ, DP, E>(p.B * C, C, s, attr);
-    // programmatic dependent launch: the verify kernel's CTAs start while the stats kernel
-    // drains; each stream waits only for its own rows' counters
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, verify_kernel<DQ, DP, E>, p);
-    if (e != cudaSuccess)   // the stats kernel ran: its counts must not reach the next call
+    e = launch_dependent(decide_kernel<DQ, DP>, p.B, 0, s, p);
+    if (e == cudaSuccess) e = launch_dependent(sweep_kernel<DQ, DP, E>, g3, sweep_smem_bytes<DQ, DP, E>(), s, p);
+    if (e == cudaSuccess) e = launch_dependent(finish_kernel<DQ, DP, E>, p.B, 0, s, p);
+    if (e != cudaSuccess)   // a kernel ran whose tickets and counters the next call must not see
         cudaMemsetAsync(p.ws, 0, workspace_bytes(p.B, p.kmax), s);
     return e;
 }
@@ -1764,7 +1795,8 @@ static cudaError_t dispatch_dtypes(VerifyParams& p, int dq, int dp, cudaStream_t
     return run_verify<__nv_bfloat16, float, E>(p, s, info);
 }
 
-static int verify_entry(const spec_verify_args* a, void* stream, int rule, const char* name, int* info) {
+// Argument checks shared by every verify entry point (no pointer is dereferenced).
+static int check_args(const spec_verify_args* a, const char* name, bool need_pointers) {
     if (a == nullptr) return set_error(SPEC_ERR_ARG, "%s: args is NULL", name);
     if (a->B < 0) return set_error(SPEC_ERR_SHAPE, "%s: B = %d < 0", name, a->B);
     if (a->V < 1 || a->V > SPEC_MAX_V)
@@ -1773,14 +1805,20 @@ static int verify_entry(const spec_verify_args* a, void* stream, int rule, const
         return set_error(SPEC_ERR_SHAPE, "%s: kmax = %d outside [0, %d]", name, a->kmax, SPEC_MAX_KMAX);
     if (!valid_dtype(a->draft_dtype) || !valid_dtype(a->target_dtype))
         return set_error(SPEC_ERR_DTYPE, "%s: dtype must be SPEC_DTYPE_F32 or SPEC_DTYPE_BF16", name);
-    if (info == nullptr) {
-        if (a->B == 0) return clear_error();
+    if (need_pointers && a->B > 0) {
         if (!a->cu_drafts || !a->target_logits || !a->temperature || !a->accepted_len || !a->out_tokens ||
             !a->n_emitted || !a->status)
             return set_error(SPEC_ERR_ARG, "%s: a required pointer is NULL", name);
         if ((a->kmax > 0) && (!a->draft_logits || !a->draft_tokens))
             return set_error(SPEC_ERR_ARG, "%s: draft_logits / draft_tokens is NULL", name);
     }
+    return SPEC_OK;
+}
+
+static int verify_entry(const spec_verify_args* a, void* stream, int rule, const char* name, int* info) {
+    int rc = check_args(a, name, info == nullptr);
+    if (rc != SPEC_OK) return rc;
+    if (info == nullptr && a->B == 0) return clear_error();
     VerifyParams p;
     p.B = a->B;
     p.V = a->V;
@@ -1801,7 +1839,10 @@ static int verify_entry(const spec_verify_args* a, void* stream, int rule, const
     const bool aligned = (a->V % 8 == 0) && ((uintptr_t)a->target_logits % 16 == 0) &&
                          ((uintptr_t)a->draft_logits % 16 == 0);
     p.nchunk = aligned ? a->V / 8 : a->V;
+    p.seg_chunks = (p.nchunk + kSegs - 1) / kSegs;
+    p.nseg = (int32_t)((p.nchunk + p.seg_chunks - 1) / p.seg_chunks);
     p.ws = reinterpret_cast<char*>(a->workspace);
+    p.list = p.ws + ((a->workspace_bytes - work_list_claims(a->B, a->kmax) * sizeof(SweepItem)) & ~(size_t)15);
     if (info == nullptr) {
         const size_t need = workspace_bytes(a->B, a->kmax);
         if (a->workspace == nullptr || a->workspace_bytes < need || (uintptr_t)a->workspace % 16 != 0)
@@ -1829,42 +1870,44 @@ extern "C" int spec_verify_block(const spec_verify_args* args, void* stream) {
 // ---------------------------------------------------------------------------------------
 // Block verification with a fixed, device-resident workspace.  Some callers cannot allocate
 // device memory at the point where they verify (an allocator that is not theirs to touch, a
-// memory budget fixed at start-up); for them the stats partials live in one array reserved
-// when the library's module is loaded, so this call allocates nothing.  The array holds
-// kStaticWorkspaceBytes: B (2 kmax + 1) row blocks (a counter and kPiecesMax 16-byte partials
-// each), i.e. up to 8192 rows (for example B = 256 at kmax = 15); larger batches are refused.
-// Like every device variable it starts zero-filled, which is the state each call leaves its
-// row counters in.  All calls share the one array, so calls that may overlap in time
-// (different streams, threads) race on it and must be ordered by the caller.
+// memory budget fixed at start-up); for them the workspace lives in one array reserved when
+// the library's module is loaded, so this call allocates nothing.  The array holds
+// kStaticWorkspaceBytes; a batch whose workspace_bytes(B, kmax) is larger is refused.  Like
+// every device variable it starts zero-filled, which is the state each call leaves it in.
+// All calls share the one array, so calls that may overlap in time (different streams,
+// threads) race on it and must be ordered by the caller.
 // ---------------------------------------------------------------------------------------
 namespace sv {
-constexpr size_t kStaticWorkspaceBytes = (size_t)8192 * kRowBytes;
+constexpr size_t kStaticWorkspaceBytes = (size_t)16 << 20;
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
-// device address of g_static_workspace on the current device, looked up once per device
+// Device address of g_static_workspace on the current device, looked up once per device and
+// kept for the life of the process (a context reset is not noticed: see the header).
 static cudaError_t static_workspace(void** ptr) {
-    static void* addr[64] = {nullptr};
+    static std::atomic<void*> addr[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (addr[dev] == nullptr) {
-        void* a = nullptr;
+    void* a = addr[dev].load(std::memory_order_acquire);
+    if (a == nullptr) {
         e = cudaGetSymbolAddress(&a, g_static_workspace);
         if (e != cudaSuccess) return e;
-        addr[dev] = a;
+        addr[dev].store(a, std::memory_order_release);   // racing first calls store the same value
     }
-    *ptr = addr[dev];
+    *ptr = a;
     return cudaSuccess;
 }
 }  // namespace sv
 
 extern "C" int spec_verify_block_static(const spec_verify_args* args, void* stream) {
     const char* name = "spec_verify_block_static";
-    if (args == nullptr) return sv::set_error(SPEC_ERR_ARG, "%s: args is NULL", name);
+    // the common checks first, so that a bad shape or dtype gets the same code as in
+    // spec_verify_block; only the workspace check is this call's own
+    int rc = sv::check_args(args, name, true);
+    if (rc != SPEC_OK) return rc;
     spec_verify_args a = *args;
-    const bool shape_ok = a.B >= 0 && a.kmax >= 0 && a.kmax <= SPEC_MAX_KMAX;
-    if (shape_ok && a.B > 0) {   // bad shapes and empty batches are reported by the common path
+    if (a.B > 0) {
         const size_t need = sv::workspace_bytes(a.B, a.kmax);
         if (need > sv::kStaticWorkspaceBytes)
             return sv::set_error(SPEC_ERR_WORKSPACE,

@@ -258,10 +258,15 @@ def test_uniforms_bit_exact_against_oracle():
         assert np.array_equal(g[..., 0], ua) and np.array_equal(g[..., 1], us)
 
 
-def _row_counters(ws):
-    """The 32-bit counter at the head of every 1040-byte row block of a workspace."""
-    n = ws.numel() // 1040
-    return ws[: n * 1040].view(n, 1040)[:, :4].contiguous().view(torch.int32).cpu().numpy()
+HEADER, ROW = 256, 1536
+
+
+def _row_counters(ws, rows):
+    """The header's tickets and the three 32-bit counters at the head of the first `rows`
+    1536-byte row blocks of a workspace (all of them zero between calls)."""
+    head = ws[:24].contiguous().view(torch.int64).cpu().numpy()
+    blocks = ws[HEADER: HEADER + rows * ROW].view(rows, ROW)[:, :12].contiguous().view(torch.int32)
+    return np.concatenate([head, blocks.cpu().numpy().reshape(-1)])
 
 
 @pytest.mark.parametrize("rule", ["tokenwise", "block"])
@@ -292,15 +297,15 @@ def test_workspace_reuse_across_batches(rule):
         got = parity.to_numpy(fn(d["cu"], d["dq"], d["dp"], d["x"], d["T"], kmax, 7, 1, out=o))
         for k in ("accepted_len", "out_tokens", "n_emitted", "status"):
             assert np.array_equal(fresh[k], got[k]), k
-        assert not _row_counters(ws).any()
+        assert not _row_counters(ws, 12 * 11).any()
     st = parity.to_numpy(fn(d_bad["cu"], d_bad["dq"], d_bad["dp"], d_bad["x"], d_bad["T"], 5, 7, 1))["status"]
     assert st[2] == 2 and st[4] == 0   # SPEC_ST_BAD_TOKEN, and the greedy stream verifies
 
 
 def test_bad_row_counter_times_out_and_heals():
-    """A row counter above its piece count (a workspace that was not zero-filled) makes the
-    stream's bounded wait give up at once with SPEC_ST_TIMEOUT; the other streams are
-    unaffected, the call resets the counter, and the next call on the workspace is exact."""
+    """A row counter that does not match its row's piece count (a workspace that was not
+    zero-filled) gives that stream SPEC_ST_TIMEOUT; the other streams are unaffected, the call
+    resets the counter, and the next call on the workspace is exact."""
     inp = workloads.make_verify_inputs("batch64", 93, B=6, N=4, V=8192)
     inp["temperature"][:] = np.maximum(inp["temperature"], 0.5)   # every stream samples
     d = parity.verify_to_device(inp, torch)
@@ -310,7 +315,7 @@ def test_bad_row_counter_times_out_and_heals():
     ws = torch.zeros(sv.spec_verify_workspace_bytes(B, 4), dtype=torch.uint8, device="cuda")
     cu = inp["cu_drafts"]
     rho = 2 * int(cu[3]) + 3                              # stream 3's first target row
-    ws[rho * 1040: rho * 1040 + 4].view(torch.int32)[0] = 1 << 20
+    ws[HEADER + rho * ROW: HEADER + rho * ROW + 4].view(torch.int32)[0] = 1 << 20
     o = {"accepted_len": torch.empty(B, dtype=torch.int32, device="cuda"),
          "out_tokens": torch.empty((B, 5), dtype=torch.int32, device="cuda"),
          "n_emitted": torch.empty(B, dtype=torch.int32, device="cuda"),
@@ -321,7 +326,27 @@ def test_bad_row_counter_times_out_and_heals():
     others = [b for b in range(B) if b != 3]
     for k in ("accepted_len", "out_tokens", "n_emitted", "status"):
         assert np.array_equal(fresh[k][others], got[k][others]), k
-    assert not _row_counters(ws).any()
+    assert not _row_counters(ws, B * 9).any()
     again = parity.to_numpy(sv.spec_verify_block(d["cu"], d["dq"], d["dp"], d["x"], d["T"], 4, 5, 2, out=o))
     for k in ("accepted_len", "out_tokens", "n_emitted", "status"):
         assert np.array_equal(fresh[k], again[k]), k
+
+
+def test_garbage_workspace_header_heals():
+    """Sweep ticket and work-list count left non-zero in the header (a workspace that was not
+    zero-filled): the call resets them before use and its results equal a fresh workspace's."""
+    inp = workloads.make_verify_inputs("batch64", 95, B=8, N=5, V=8192)
+    d = parity.verify_to_device(inp, torch)
+    fresh = parity.to_numpy(sv.spec_verify_block(d["cu"], d["dq"], d["dp"], d["x"], d["T"], 5, 3, 4))
+    B = 8
+    ws = torch.zeros(sv.spec_verify_workspace_bytes(B, 5), dtype=torch.uint8, device="cuda")
+    ws[8:24].view(torch.int64)[:] = torch.tensor([123456789, 987654321], dtype=torch.int64, device="cuda")
+    o = {"accepted_len": torch.empty(B, dtype=torch.int32, device="cuda"),
+         "out_tokens": torch.empty((B, 6), dtype=torch.int32, device="cuda"),
+         "n_emitted": torch.empty(B, dtype=torch.int32, device="cuda"),
+         "status": torch.empty(B, dtype=torch.int32, device="cuda"),
+         "workspace": ws}
+    got = parity.to_numpy(sv.spec_verify_block(d["cu"], d["dq"], d["dp"], d["x"], d["T"], 5, 3, 4, out=o))
+    for k in ("accepted_len", "out_tokens", "n_emitted", "status"):
+        assert np.array_equal(fresh[k], got[k]), k
+    assert not _row_counters(ws, B * 11).any()

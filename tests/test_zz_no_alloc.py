@@ -27,9 +27,18 @@ def _fake_args(B, kmax):
 
 def test_static_workspace_capacity_is_checked_on_the_host():
     L = sv.lib()
-    # 256 streams x (2 * 16 + 1) rows = 8448 rows > 8192: refused, nothing launched
-    assert L.spec_verify_block_static(ctypes.byref(_fake_args(256, 16)), None) == SPEC_ERR_WORKSPACE
+    # 512 streams x (2 * 16 + 1) rows need 35 MB > the 16 MiB array: refused, nothing launched
+    assert sv.spec_verify_workspace_bytes(512, 16) > 16 << 20
+    assert L.spec_verify_block_static(ctypes.byref(_fake_args(512, 16)), None) == SPEC_ERR_WORKSPACE
     assert b"static workspace" in L.spec_last_error()
+    # an oversized batch with a bad dtype or V gets spec_verify_block's code for it: the
+    # argument checks come before the capacity check
+    a = _fake_args(512, 16)
+    a.draft_dtype = 7
+    assert L.spec_verify_block_static(ctypes.byref(a), None) == -2
+    a = _fake_args(512, 16)
+    a.V = 0
+    assert L.spec_verify_block_static(ctypes.byref(a), None) == -3
     # shape errors and empty batches take the common path's answers
     assert L.spec_verify_block_static(ctypes.byref(_fake_args(4, 33)), None) == -3
     assert L.spec_verify_block_static(ctypes.byref(_fake_args(0, 5)), None) == 0
@@ -46,8 +55,9 @@ def test_static_matches_caller_workspace_on_consecutive_calls(case):
     from tests import parity
     if case == "batch64_small":
         inp = workloads.make_verify_inputs("batch64", 8100, B=24, V=8192)
-    else:   # 256 streams x 31 rows = 7936 rows, just under the 8192-row capacity
+    else:   # 256 streams x 31 rows: 15.6 MiB of workspace, just under the 16 MiB array
         inp = workloads.make_verify_inputs("batch64", 8200, B=256, N=15, V=1024)
+        assert 15 << 20 < sv.spec_verify_workspace_bytes(256, 15) <= 16 << 20
     d = parity.verify_to_device(inp, torch)
     kmax = inp["kmax"]
     for step in (0, 1):   # two consecutive calls on the same fixed workspace
