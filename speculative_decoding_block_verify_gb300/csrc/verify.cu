@@ -91,10 +91,11 @@ struct Part {
 // must be zero between calls (tickets, counters) sits at the same place for every B, and every
 // call returns it to zero, so a zero-filled workspace stays valid from call to call.
 // ---------------------------------------------------------------------------------------
+constexpr int kTailTickets = 8;        // the stats tail is cut into this many claim ranges
 struct WsHeader {
-    unsigned long long reserved;       // zero
     unsigned long long ticket_sweep;   // next sweep claim
     unsigned long long sweep_total;    // sweep claims appended by decide_kernel
+    unsigned long long ticket_stats[kTailTickets];   // next piece of each range of the stats tail
     int32_t L;                         // streams [0, L) have valid offsets
 };
 struct RowStat {
@@ -775,18 +776,34 @@ __device__ __forceinline__ int stream_of_row(const VerifyParams& p, int64_t rho,
     return lo;
 }
 
-// Chunks per warp of the stats kernel: equal shares of all rows' chunks, but at least
-// ceil(n / (kPiecesMax - 2)) so that no row is cut into more than kPiecesMax pieces.
+// The stats kernel's work: the first rows (the static rows) in equal contiguous shares, one per
+// warp; the remaining rows in fixed pieces of two segments, claimed by whichever warp is free
+// (so SMs that run slower, or whose CTAs started later, simply take fewer of them).  The claimed
+// tail pays a ramp and a claim per piece, which only a long share amortises: measured on the
+// batch-64 bf16 call (~50 KB per warp) any tail costs more than the end-time spread it removes,
+// on the batch-256 fp32 call (~690 KB per warp) a fifth of the rows as tail saves ~10%.  So the
+// tail is a fifth of the rows when a warp's share is at least kTailMinChunks chunks, else empty.
+constexpr int64_t kTailMinChunks = 16384;
+__host__ __device__ inline int64_t static_rows(int64_t rows, int64_t n, int64_t warps) {
+    return (rows * n >= kTailMinChunks * warps) ? rows * 4 / 5 : rows;
+}
+__host__ __device__ inline int64_t tail_pieces_per_row(int64_t n, int64_t seg_chunks) {
+    const int64_t pc = 2 * seg_chunks;
+    return (n + pc - 1) / pc;
+}
+// Chunks per warp of the static rows: equal shares, but at least ceil(n / (kPiecesMax - 2)) so
+// that no row is cut into more than kPiecesMax pieces.
 __host__ __device__ inline int64_t stats_share(int64_t rows, int64_t n, int64_t nw) {
     const int64_t lw = (rows * n + nw - 1) / nw;
     const int64_t lmin = (n + kPiecesMax - 3) / (kPiecesMax - 2);
     return lw > lmin ? lw : (lmin > 0 ? lmin : 1);
 }
-// The pieces of stats row rho: warps first .. first + count - 1; warp gw's partial is piece
-// gw - first of the row.
-__device__ __forceinline__ void row_pieces(int64_t rho, int64_t n, int64_t lw, int64_t& first, int& count) {
-    first = rho * n / lw;
-    count = (int)((rho * n + n - 1) / lw - first) + 1;
+// The pieces of stats row rho.  A static row (rho < rs): warps first .. first + count - 1,
+// warp gw's partial is piece gw - first; a tail row: tail_pieces_per_row fixed pieces.
+__device__ __forceinline__ int row_piece_count(int64_t rho, int64_t n, int64_t lw, int64_t rs, int64_t seg_chunks) {
+    if (rho >= rs) return (int)tail_pieces_per_row(n, seg_chunks);
+    const int64_t first = rho * n / lw;
+    return (int)((rho * n + n - 1) / lw - first) + 1;
 }
 
 template <typename DQ, typename DP, int E>
@@ -809,22 +826,17 @@ __global__ void __launch_bounds__(kStatsThreads, 768 / kStatsThreads) stats_kern
     if (L == 0) return;
     const int64_t n = p.nchunk;
     const int64_t rows = 2 * (int64_t)p.cu[L] + L;
-    const int64_t lw = stats_share(rows, n, p.stats_warps);
+    const int64_t rs = static_rows(rows, n, p.stats_warps);
+    const int64_t lw = stats_share(rs, n, p.stats_warps);
     const int64_t gw = (int64_t)blockIdx.x * kStatsWarps + warp;
-    int64_t f = gw * lw;
-    const int64_t f1 = min(f + lw, rows * n);
-    if (f >= f1) return;
-    int64_t rho = f / n;
-    int64_t c = f - rho * n;
-    int b = stream_of_row(p, rho, 0, L);
-    int64_t gb = 2 * (int64_t)p.cu[b] + b;
-    int Nb = p.cu[b + 1] - p.cu[b];
     const int64_t V = p.V;
-    auto nothing = []() {};
-    while (f < f1) {
-        const int64_t c_end = min(n, c + (f1 - f));
-        while (rho - gb > 2 * (int64_t)Nb) {
-            ++b;
+    int b = 0;
+    int64_t gb = 0;
+    int Nb = p.cu[1] - p.cu[0];
+    // one piece [c, c_end) of row rho into partial slot `slot`
+    auto piece = [&](int64_t rho, int64_t c, int64_t c_end, int slot, auto after_last) {
+        if (rho > gb + 2 * (int64_t)Nb) {   // rows only move forward for a warp
+            b = stream_of_row(p, rho, b, L);
             gb = 2 * (int64_t)p.cu[b] + b;
             Nb = p.cu[b + 1] - p.cu[b];
         }
@@ -832,27 +844,80 @@ __global__ void __launch_bounds__(kStatsThreads, 768 / kStatsThreads) stats_kern
         const float T = p.temp[b];
         const bool greedy = (T == 0.f);
         const bool draft = j > Nb;
-        const bool skip = !temperature_ok(T) || (draft && greedy);
-        if (!skip) {
-            float ah = 0.f, al = 0.f;
-            if (!greedy) {
-                const df a = scale_of_temperature(T);
-                ah = a.hi;
-                al = a.lo;
-            }
-            char* blk = row_block(p, rho);
-            Part* dst = blk_at<Part>(blk, kOffParts) + (gw - rho * n / lw);
-            if (draft)
-                stats_piece<DQ, E>(ring, row_ptr<DQ>(p.dq, (int64_t)p.cu[b] + (j - Nb - 1), V), c, c_end, false, ah,
-                                   al, lane, dst, nothing);
-            else
-                stats_piece<DP, E>(ring, row_ptr<DP>(p.dp, (int64_t)p.cu[b] + b + j, V), c, c_end, greedy, ah, al,
-                                   lane, dst, nothing);
-            if (lane == 0) atomicAdd(blk_at<unsigned>(blk, kOffStatsCount), 1u);   // after lane 0's partial
+        if (!temperature_ok(T) || (draft && greedy)) {   // never read
+            after_last();
+            return;
         }
-        f += c_end - c;
-        c = 0;
-        ++rho;
+        float ah = 0.f, al = 0.f;
+        if (!greedy) {
+            const df a = scale_of_temperature(T);
+            ah = a.hi;
+            al = a.lo;
+        }
+        char* blk = row_block(p, rho);
+        Part* dst = blk_at<Part>(blk, kOffParts) + slot;
+        if (draft)
+            stats_piece<DQ, E>(ring, row_ptr<DQ>(p.dq, (int64_t)p.cu[b] + (j - Nb - 1), V), c, c_end, false, ah, al,
+                               lane, dst, after_last);
+        else
+            stats_piece<DP, E>(ring, row_ptr<DP>(p.dp, (int64_t)p.cu[b] + b + j, V), c, c_end, greedy, ah, al, lane,
+                               dst, after_last);
+        if (lane == 0) atomicAdd(blk_at<unsigned>(blk, kOffStatsCount), 1u);   // after lane 0's partial
+    };
+    auto nothing = []() {};
+    // ---- this warp's static share
+    int64_t f = gw * lw;
+    const int64_t f1 = min(f + lw, rs * n);
+    if (f < f1) {
+        int64_t rho = f / n;
+        int64_t c = f - rho * n;
+        while (f < f1) {
+            const int64_t c_end = min(n, c + (f1 - f));
+            piece(rho, c, c_end, (int)(gw - rho * n / lw), nothing);
+            f += c_end - c;
+            c = 0;
+            ++rho;
+        }
+    }
+    // ---- the tail: fixed pieces claimed one by one from kTailTickets ranges (a warp starts on
+    // its own range and moves on when it is used up, so no single counter takes every claim; a
+    // plain read skips a used-up range without an atomic).  The next claim is fired once the
+    // current piece's last copy is issued, so its round trip overlaps the piece's last stages.
+    const int64_t pc = 2 * p.seg_chunks;
+    const int64_t npd = tail_pieces_per_row(n, p.seg_chunks);
+    const unsigned long long total = (unsigned long long)(rows - rs) * (unsigned long long)npd;
+    const unsigned long long per_range = (total + kTailTickets - 1) / kTailTickets;
+    const int home = (int)(gw % kTailTickets);
+    unsigned long long next = total;
+    auto claim = [&]() {   // all lanes: lanes 0..kTailTickets-1 read one ticket each (one round trip)
+        const int rg = (home + lane) % kTailTickets;
+        const unsigned long long lo = (unsigned long long)rg * per_range;
+        const unsigned long long span = (lo < total) ? min(per_range, total - lo) : 0ull;
+        const bool open = lane < kTailTickets && __ldcg(&hdr->ticket_stats[rg]) < span;
+        unsigned mask = __ballot_sync(0xffffffffu, open);
+        next = total;
+        while (mask) {   // the first open range, from this warp's home range on
+            const int l = __ffs(mask) - 1;
+            unsigned long long got = 0;
+            if (lane == l) got = atomicAdd(&hdr->ticket_stats[rg], 1ull);
+            got = __shfl_sync(0xffffffffu, got, l);
+            const unsigned long long lo_l = __shfl_sync(0xffffffffu, lo, l);
+            const unsigned long long span_l = __shfl_sync(0xffffffffu, span, l);
+            if (got < span_l) {
+                next = lo_l + got;
+                break;
+            }
+            mask &= mask - 1;
+        }
+    };
+    claim();
+    unsigned long long cur = __shfl_sync(0xffffffffu, next, 0);
+    while (cur < total) {
+        const int64_t rho = rs + (int64_t)(cur / (unsigned long long)npd);
+        const int k = (int)(cur % (unsigned long long)npd);
+        const int64_t c = (int64_t)k * pc;
+        piece(rho, c, min(n, c + pc), k, claim);
+        cur = __shfl_sync(0xffffffffu, next, 0);
     }
     // no TMA copy of this warp may still be writing its ring when the CTA leaves
     ring.drain();
@@ -924,7 +989,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const VerifyParams p) 
     WsHeader* hdr = ws_header(p);
     if (!offsets_ok) return;   // finish_kernel reports BAD_OFFSETS
     const int L = __ldcg(&hdr->L);
-    const int64_t lw = stats_share(2 * (int64_t)p.cu[L] + L, p.nchunk, p.stats_warps);
+    const int64_t rs = static_rows(2 * (int64_t)p.cu[L] + L, p.nchunk, p.stats_warps);
+    const int64_t lw = stats_share(rs, p.nchunk, p.stats_warps);
     const int64_t gb = 2 * (int64_t)base + b;
     const int nrows = 2 * N + 1;
     const bool reduce_rows = temp_ok && !bad_tok;
@@ -936,9 +1002,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const VerifyParams p) 
         for (int r = (greedy ? N : 0) + warp; r < nrows; r += kWarps) {
             const int64_t rho = stats_row_of_part(gb, N, r);
             char* blk = row_block(p, rho);
-            int64_t first;
-            int cnt_want;
-            row_pieces(rho, p.nchunk, lw, first, cnt_want);
+            const int cnt_want = row_piece_count(rho, p.nchunk, lw, rs, p.seg_chunks);
             const unsigned cnt = __ldcg(blk_at<unsigned>(blk, kOffStatsCount));
             Part e[2];
 #pragma unroll
@@ -1413,7 +1477,8 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) 
     const int n_raw = p.cu[b + 1] - base;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     WsHeader* hdr = ws_header(p);
-    if (b == 0 && tid == 0) {   // the sweep grid has finished: its ticket and list go back to zero
+    if (b == 0 && tid == 0) {   // every earlier grid of the call has finished: tickets back to zero
+        for (int i = 0; i < kTailTickets; ++i) hdr->ticket_stats[i] = 0ull;
         hdr->ticket_sweep = 0ull;
         hdr->sweep_total = 0ull;
     }

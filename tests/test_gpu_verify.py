@@ -262,9 +262,10 @@ HEADER, ROW = 256, 1536
 
 
 def _row_counters(ws, rows):
-    """The header's tickets and the three 32-bit counters at the head of the first `rows`
+    """The header's tickets (the sweep's ticket and count, the stats tail's eight tickets) and
+    the three 32-bit counters at the head of the first `rows`
     1536-byte row blocks of a workspace (all of them zero between calls)."""
-    head = ws[:24].contiguous().view(torch.int64).cpu().numpy()
+    head = ws[:80].contiguous().view(torch.int64).cpu().numpy()
     blocks = ws[HEADER: HEADER + rows * ROW].view(rows, ROW)[:, :12].contiguous().view(torch.int32)
     return np.concatenate([head, blocks.cpu().numpy().reshape(-1)])
 
@@ -340,7 +341,7 @@ def test_garbage_workspace_header_heals():
     fresh = parity.to_numpy(sv.spec_verify_block(d["cu"], d["dq"], d["dp"], d["x"], d["T"], 5, 3, 4))
     B = 8
     ws = torch.zeros(sv.spec_verify_workspace_bytes(B, 5), dtype=torch.uint8, device="cuda")
-    ws[8:24].view(torch.int64)[:] = torch.tensor([123456789, 987654321], dtype=torch.int64, device="cuda")
+    ws[0:16].view(torch.int64)[:] = torch.tensor([123456789, 987654321], dtype=torch.int64, device="cuda")
     o = {"accepted_len": torch.empty(B, dtype=torch.int32, device="cuda"),
          "out_tokens": torch.empty((B, 6), dtype=torch.int32, device="cuda"),
          "n_emitted": torch.empty(B, dtype=torch.int32, device="cuda"),
