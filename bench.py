@@ -133,11 +133,12 @@ def _oracle_task(args):
     x = np.asarray(inp["draft_tokens"][cu[b]:cu[b] + n])
     T = float(inp["temperature"][b])
     if T == 0.0:   # greedy streams are not part of the sample
-        return 0.0, 0
+        return 0.0, 0, 0, 0
     t0 = time.perf_counter()
+    ties = 0
     for st in steps:
-        ov.verify_stream(rule, q_rows, p_rows, x, T, 0, st, b)
-    return time.perf_counter() - t0, len(steps) * len(x)
+        ties += int(ov.verify_stream(rule, q_rows, p_rows, x, T, 0, st, b)["tie"])
+    return time.perf_counter() - t0, len(steps) * len(x), ties, len(steps)
 
 
 def oracle_pool():
@@ -177,9 +178,11 @@ def oracle_sample(n_verifies, rule, seed=3000, pool=None):
             pool.join()
     cpu_s = sum(x[0] for x in res)
     slots = sum(x[1] for x in res)
+    ties, verifies = sum(x[2] for x in res), sum(x[3] for x in res)
     return {"value": slots / wall, "unit": UNIT, "cores": min(cores, len(split)), "kind": "oracle",
             "sample": f"the sampled streams among 16 x {per} steps of the batch-64 workload (k=5, V=129280), "
-                      f"{rule} rule, float64 NumPy, {cpu_s:.1f} s of CPU work in {wall:.1f} s wall"}
+                      f"{rule} rule, float64 NumPy, {cpu_s:.1f} s of CPU work in {wall:.1f} s wall",
+            "near_tie_streams": ties, "stream_verifies": verifies}
 
 
 # ---------------------------------------------------------------------------------------
@@ -392,7 +395,7 @@ def run_ours(a, dist):
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": elapsed_ms / a.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accum_dtype": "f32",
         "data": "synthetic (seeded torch generator on the device; bf16 logits)",
         "config": {"workload": f"{HEADLINE}: B=64 streams, k=5 drafts + 1 bonus, V=129280, bf16 logits, "
                                f"{a.rule} verification",
@@ -411,6 +414,8 @@ def run_ours(a, dist):
     }
     if not a.no_secondary and dist.rank == 0:
         result["secondary"] = secondary(sv, workloads, torch, dev)
+        result["acceptance"] = [acceptance(sv, workloads, torch, dev, HEADLINE, 3000, a.rule),
+                                acceptance(sv, workloads, torch, dev, "batch256_k9", 6000, "block", steps=5)]
     return result
 
 
@@ -516,7 +521,56 @@ def secondary(sv, workloads, torch, dev):
         "pipeline_us_per_step": ms_ad * 1e3, "drafts_verified_per_step": int(kk.sum()),
         "k_histogram": np.bincount(kk, minlength=6).tolist(),
         "slots_per_s": int(kk.sum()) / (ms_ad / 1e3)}
+    del vin
+    torch.cuda.empty_cache()
+    # the same step as one CUDA graph (pick -> verify of each stream's first k_b drafts ->
+    # acceptance counters -> step + 1), on the dense draft/target layout the drafter fills
+    dn = workloads.make_verify_inputs("adaptive128", 13, backend="torch", device=dev)   # k = 5 everywhere
+    B, K, V = 128, 5, dn["V"]
+    pl = sv.SpecPipeline(h, w, 0.0, vm, dn["draft_logits"].view(B, K, V), dn["target_logits"].view(B, K + 1, V),
+                         dn["draft_tokens"].view(B, K), dn["temperature"], rule=1)
+    ms_graph = _time(lambda i: pl.launch(), 30, stream)
+    a_p, marg, tps = sv.acceptance_rates(pl.counts, K)
+    res["adaptive128_graph"] = {
+        "graph_us_per_step": ms_graph * 1e3,
+        "eager_us_per_step": ms_ad * 1e3,
+        "drafts_verified_per_step": int(pl.out["k"].sum().item()),
+        "a_p": a_p, "tokens_per_step": tps}
+    pl.close()
+    del dn, pl
+    torch.cuda.empty_cache()
+    # the tiny configuration's latency (B = 1, k = 5, V = 1024, fp32)
+    tiny = workloads.make_verify_inputs("tiny", 1000, backend="torch", device=dev)
+    to = sv.spec_verify_block(tiny["cu_drafts"], tiny["draft_logits"], tiny["target_logits"], tiny["draft_tokens"],
+                              tiny["temperature"], 5, 0, 0)
+
+    def tiny_call(i):
+        sv.spec_verify_block(tiny["cu_drafts"], tiny["draft_logits"], tiny["target_logits"], tiny["draft_tokens"],
+                             tiny["temperature"], 5, 0, i, out=to)
+    res["tiny_block_latency_us"] = _time(tiny_call, 200, stream) * 1e3
     return res
+
+
+def acceptance(sv, workloads, torch, dev, name, seed, rule, steps=30):
+    """Per-position acceptance a_p, the marginal a_p / a_{p-1}, tokens per step = 1 + sum a_p
+    (P1 §6) and the status counts of `steps` untimed calls on the workload."""
+    import numpy as np
+    inp = workloads.make_verify_inputs(name, seed, backend="torch", device=dev)
+    k = inp["kmax"]
+    fn = sv.spec_verify_block if rule == "block" else sv.spec_verify_tokenwise
+    counts, status = None, np.zeros(8, np.int64)
+    out = None
+    for i in range(steps):
+        out = fn(inp["cu_drafts"], inp["draft_logits"], inp["target_logits"], inp["draft_tokens"],
+                 inp["temperature"], k, 0, i, out=out)
+        counts = sv.spec_accept_counters(out["accepted_len"], out["status"], inp["cu_drafts"], k, counts)
+        status += np.bincount(out["status"].cpu().numpy(), minlength=8)[:8]
+    a_p, marg, tps = sv.acceptance_rates(counts, k)
+    del inp
+    torch.cuda.empty_cache()
+    return {"workload": name, "rule": rule, "steps": steps, "a_p": a_p, "marginal": marg,
+            "tokens_per_step": tps,
+            "status_counts": {sv.STATUS_NAMES[j]: int(status[j]) for j in range(8) if status[j]}}
 
 
 def run_reference(a, dist):

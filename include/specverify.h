@@ -246,6 +246,84 @@ int adaptive_pick_k(const void* hidden, const void* w, int32_t dtype, float bias
                     int32_t* cu_drafts_out, void* stream);
 
 /*
+ * spec_accept_counters - per-position acceptance counts of a batch's verify results.
+ * [P1] §6 "The arithmetic you need before tuning k": a_p, the share of steps whose p-th
+ * draft was accepted, and tokens per step = 1 + sum_p a_p (the emitted tokens tau + 1).
+ * Adds to counts [2 kmax + 1] (uint64, device, accumulated over calls; zero it to start):
+ *   counts[0]        += streams with status SPEC_ST_OK (the steps);
+ *   counts[p]        += OK streams with accepted_len >= p, p = 1..kmax (accepted at p);
+ *   counts[kmax + p] += OK streams that verified at least p drafts (offered at p).
+ * a_p = counts[p] / counts[0]; the marginal rate a_p / a_{p-1}; tokens per step
+ * 1 + sum_p a_p.  accepted_len, status [B] and cu_drafts [B + 1] as written / read by a
+ * verify call.  Errors: SPEC_ERR_ARG (NULL pointer), SPEC_ERR_SHAPE (B < 0, kmax outside
+ * [0, SPEC_MAX_KMAX]), SPEC_ERR_CUDA.  B == 0 launches nothing.
+ */
+int spec_accept_counters(const int32_t* accepted_len, const int32_t* status, const int32_t* cu_drafts,
+                         int32_t B, int32_t kmax, uint64_t* counts, void* stream);
+
+/*
+ * The adaptive verify step as one CUDA graph: adaptive_pick_k (confidence head, prefix
+ * survival, k_b per stream and the offsets cu_drafts_out) -> the verify of each stream's
+ * first k_b drafts -> spec_accept_counters -> *step += 1.  [P1] §3 "The Markov fix-up" (the
+ * sampling runs inside the same CUDA graph as the draft pass) and "Two cliffs, not one" (one
+ * graph per batch size); [P3] "The controller, and the table it reads from" (the controller
+ * picks how many drafts each stream verifies).
+ * Layout: the drafter fills all kmax slots of every stream and the target scores all of
+ * them, so draft_logits is [B, kmax, V] (row b kmax + i), target_logits [B, kmax + 1, V]
+ * (row b (kmax + 1) + i, i <= k_b, row b (kmax + 1) + k_b is the bonus slot of the k_b
+ * verified drafts), draft_tokens [B, kmax]; a stream verifies its first k_b drafts.
+ * The Philox step of each launch is read from the device word *step (uint64), which the
+ * graph increments at its end; every other argument is fixed at creation (device pointers
+ * must stay valid while the pipeline lives; outputs as in adaptive_pick_k and the verify
+ * calls, diag [B (kmax + 1), SPEC_DIAG_COLS] in the dense target-row order; accept_counts may
+ * be NULL).  The workspace (spec_verify_workspace_bytes(B, kmax), zero-filled once) belongs
+ * to the pipeline while it lives; launches of one pipeline must be ordered (one stream).
+ */
+typedef struct {
+    /* confidence head and controller (see adaptive_pick_k) */
+    const void* hidden;        /* [B, kmax, H] */
+    const void* w;             /* [H] */
+    int32_t head_dtype;
+    float bias;
+    int32_t H;
+    const float* verify_ms;    /* [n_max + 1] */
+    int32_t n_max;
+    int32_t mode;              /* 0 per stream, 1 batch-greedy */
+    /* verification */
+    int32_t rule;              /* 0 token-wise, 1 block */
+    int32_t B, V, kmax;
+    const void* draft_logits;  /* [B, kmax, V] */
+    int32_t draft_dtype;
+    const void* target_logits; /* [B, kmax + 1, V] */
+    int32_t target_dtype;
+    const int32_t* draft_tokens;   /* [B, kmax] */
+    const float* temperature;      /* [B] */
+    uint64_t seed;
+    uint64_t* step;            /* device, 1 word: this launch's step; incremented by the graph */
+    /* outputs */
+    float* c_out;              /* [B, kmax] */
+    float* a_out;              /* [B, kmax] */
+    int32_t* k_out;            /* [B] */
+    int32_t* cu_drafts_out;    /* [B + 1] */
+    int32_t* accepted_len;     /* [B] */
+    int32_t* out_tokens;       /* [B, kmax + 1] */
+    int32_t* n_emitted;        /* [B] */
+    int32_t* status;           /* [B] */
+    float* diag;               /* optional */
+    uint64_t* accept_counts;   /* optional [2 kmax + 1], accumulated */
+    void* workspace;
+    size_t workspace_bytes;
+} spec_pipeline_args;
+
+/* Capture the graph (nothing runs yet).  *pipeline receives an opaque handle.  Errors: those
+ * of adaptive_pick_k and the verify calls, SPEC_ERR_ARG (NULL pointer, rule not 0/1). */
+int spec_pipeline_create(const spec_pipeline_args* args, void** pipeline);
+/* Run one step: one graph launch on `stream`. */
+int spec_pipeline_launch(void* pipeline, void* stream);
+/* Release the graph (NULL is accepted). */
+int spec_pipeline_destroy(void* pipeline);
+
+/*
  * spec_philox_uniforms - the verify calls' uniforms, exposed for checking.
  * out [n_streams, n_slots, 2] double: (acceptance uniform, sampling uniform) of every
  * (stream, slot) for the given seed and step, exactly as the verify kernels draw them.

@@ -11,6 +11,8 @@ Entry points (same names as the C ABI):
 * ``spec_verify_tokenwise``  - token-by-token speculative sampling
 * ``spec_verify_block``      - block verification
 * ``adaptive_pick_k``        - confidence head + pick how many drafts to verify
+* ``spec_accept_counters``   - per-position acceptance counts (a_p, tokens per step)
+* ``SpecPipeline``           - pick k -> ragged verify -> counters as one CUDA graph
 * ``spec_philox_uniforms``   - the verify calls' uniforms (for checking)
 
 Build the library first: ``python -m speculative_decoding_block_verify_gb300.build`` (or
@@ -22,6 +24,7 @@ import os
 
 __all__ = [
     "dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block", "adaptive_pick_k",
+    "spec_accept_counters", "acceptance_rates", "SpecPipeline",
     "spec_philox_uniforms", "spec_verify_launch_info",
     "spec_verify_workspace_bytes", "spec_verify_block_static", "lib", "lib_path", "SpecError",
     "DTYPE_F32", "DTYPE_BF16", "STATUS_NAMES", "DIAG_COLS",
@@ -35,7 +38,8 @@ STATUS_NAMES = {0: "OK", 1: "BAD_TEMPERATURE", 2: "BAD_TOKEN", 3: "BAD_ROW",
 EXPORTED = ["dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block",
             "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info",
             "spec_verify_workspace_bytes", "spec_verify_block_static",
-            "spec_last_error", "spec_version"]
+            "spec_accept_counters", "spec_pipeline_create", "spec_pipeline_launch",
+            "spec_pipeline_destroy", "spec_last_error", "spec_version"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -65,6 +69,25 @@ class VerifyArgs(ctypes.Structure):
     ]
 
 
+class PipelineArgs(ctypes.Structure):
+    """Mirror of spec_pipeline_args."""
+    _fields_ = [
+        ("hidden", ctypes.c_void_p), ("w", ctypes.c_void_p), ("head_dtype", ctypes.c_int32),
+        ("bias", ctypes.c_float), ("H", ctypes.c_int32), ("verify_ms", ctypes.c_void_p),
+        ("n_max", ctypes.c_int32), ("mode", ctypes.c_int32),
+        ("rule", ctypes.c_int32), ("B", ctypes.c_int32), ("V", ctypes.c_int32), ("kmax", ctypes.c_int32),
+        ("draft_logits", ctypes.c_void_p), ("draft_dtype", ctypes.c_int32),
+        ("target_logits", ctypes.c_void_p), ("target_dtype", ctypes.c_int32),
+        ("draft_tokens", ctypes.c_void_p), ("temperature", ctypes.c_void_p),
+        ("seed", ctypes.c_uint64), ("step", ctypes.c_void_p),
+        ("c_out", ctypes.c_void_p), ("a_out", ctypes.c_void_p), ("k_out", ctypes.c_void_p),
+        ("cu_drafts_out", ctypes.c_void_p), ("accepted_len", ctypes.c_void_p),
+        ("out_tokens", ctypes.c_void_p), ("n_emitted", ctypes.c_void_p), ("status", ctypes.c_void_p),
+        ("diag", ctypes.c_void_p), ("accept_counts", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
 def lib_path():
     return os.path.join(_HERE, "_build", "libspecverify.so")
 
@@ -89,12 +112,18 @@ def lib():
     L.spec_philox_uniforms.argtypes = [u64, u64, i32, i32, vp, vp]
     L.spec_verify_launch_info.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.POINTER(i32),
                                           ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    L.spec_accept_counters.argtypes = [vp, vp, vp, i32, i32, vp, vp]
+    L.spec_pipeline_create.argtypes = [ctypes.POINTER(PipelineArgs), ctypes.POINTER(vp)]
+    L.spec_pipeline_launch.argtypes = [vp, vp]
+    L.spec_pipeline_destroy.argtypes = [vp]
     L.spec_verify_workspace_bytes.argtypes = [i32, i32]
     L.spec_verify_workspace_bytes.restype = ctypes.c_size_t
     L.spec_last_error.restype = ctypes.c_char_p
     L.spec_version.restype = ctypes.c_int32
     for name in ("dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block", "spec_verify_block_static",
-                 "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info"):
+                 "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info",
+                 "spec_accept_counters", "spec_pipeline_create", "spec_pipeline_launch",
+                 "spec_pipeline_destroy"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -270,6 +299,112 @@ def adaptive_pick_k(hidden, w, bias, verify_ms, mode=0, out=None, stream=None):
                                  _ptr(out["c"]), _ptr(out["a"]), _ptr(out["k"]), _ptr(out["cu"]),
                                  _stream(stream)))
     return out
+
+
+def spec_accept_counters(accepted_len, status, cu_drafts, kmax, counts=None, stream=None):
+    """Adds one batch's per-position acceptance counts to ``counts`` [2 kmax + 1] (uint64 as
+    int64, device; allocated zeroed when None) and returns it: counts[0] = verified streams,
+    counts[p] = accepted at position p, counts[kmax + p] = offered at position p."""
+    torch = _torch()
+    _dev(accepted_len, "accepted_len", torch.int32)
+    _dev(status, "status", torch.int32)
+    _dev(cu_drafts, "cu_drafts", torch.int32)
+    B = status.numel()
+    if counts is None:
+        counts = torch.zeros(2 * kmax + 1, dtype=torch.int64, device=status.device)
+    _dev(counts, "counts", torch.int64)
+    if counts.numel() != 2 * kmax + 1:
+        raise ValueError("counts must have 2 kmax + 1 entries")
+    _check(lib().spec_accept_counters(_ptr(accepted_len), _ptr(status), _ptr(cu_drafts), B, kmax,
+                                      _ptr(counts), _stream(stream)))
+    return counts
+
+
+def acceptance_rates(counts, kmax):
+    """(a_p for p = 1..kmax, marginal a_p / a_{p-1}, tokens per step = 1 + sum a_p) from the
+    accumulated counts (P1 §6 "The arithmetic you need before tuning k")."""
+    c = [int(v) for v in counts.cpu().tolist()]
+    steps = max(c[0], 1)
+    a = [c[p] / steps for p in range(1, kmax + 1)]
+    marg = [a[0]] + [(a[p] / a[p - 1]) if a[p - 1] > 0 else 0.0 for p in range(1, kmax)]
+    return a, marg, 1.0 + sum(a)
+
+
+class SpecPipeline:
+    """pick k -> verify each stream's first k_b drafts -> acceptance counters -> step + 1, as
+    one CUDA graph (spec_pipeline_create / launch / destroy).  Inputs are the dense layout:
+    draft_logits [B, kmax, V], target_logits [B, kmax + 1, V], draft_tokens [B, kmax]; the
+    confidence head's hidden [B, kmax, H], w [H] and verify_ms [n_max + 1].  ``step`` is the
+    first launch's Philox step; each launch adds 1.  The outputs (``out`` dict) and the
+    counters are device tensors that every launch overwrites (counters accumulate)."""
+
+    def __init__(self, hidden, w, bias, verify_ms, draft_logits, target_logits, draft_tokens,
+                 temperature, rule=1, mode=0, seed=0, step=0, diag=False, counters=True):
+        torch = _torch()
+        for t, n in ((hidden, "hidden"), (w, "w"), (draft_logits, "draft_logits"),
+                     (target_logits, "target_logits")):
+            _dev(t, n)
+        _dev(verify_ms, "verify_ms", torch.float32)
+        _dev(draft_tokens, "draft_tokens", torch.int32)
+        _dev(temperature, "temperature", torch.float32)
+        B, kmax, V = draft_logits.shape
+        if tuple(target_logits.shape) != (B, kmax + 1, V) or tuple(draft_tokens.shape) != (B, kmax):
+            raise ValueError("target_logits must be [B, kmax + 1, V] and draft_tokens [B, kmax]")
+        if hidden.shape[:2] != (B, kmax) or w.shape != (hidden.shape[2],) or w.dtype != hidden.dtype:
+            raise ValueError("hidden must be [B, kmax, H] and w [H] of hidden's dtype")
+        dev = draft_logits.device
+        self.kmax = kmax
+        self.out = {
+            "c": torch.empty((B, kmax), dtype=torch.float32, device=dev),
+            "a": torch.empty((B, kmax), dtype=torch.float32, device=dev),
+            "k": torch.empty(B, dtype=torch.int32, device=dev),
+            "cu": torch.empty(B + 1, dtype=torch.int32, device=dev),
+            "accepted_len": torch.empty(B, dtype=torch.int32, device=dev),
+            "out_tokens": torch.empty((B, kmax + 1), dtype=torch.int32, device=dev),
+            "n_emitted": torch.empty(B, dtype=torch.int32, device=dev),
+            "status": torch.empty(B, dtype=torch.int32, device=dev),
+        }
+        if diag:
+            self.out["diag"] = torch.empty((B * (kmax + 1), DIAG_COLS), dtype=torch.float32, device=dev)
+        self.counts = torch.zeros(2 * kmax + 1, dtype=torch.int64, device=dev) if counters else None
+        self.step = torch.tensor([int(step)], dtype=torch.int64, device=dev)
+        self.workspace = torch.zeros(max(spec_verify_workspace_bytes(B, kmax), 16), dtype=torch.uint8,
+                                     device=dev)
+        self._keep = (hidden, w, verify_ms, draft_logits, target_logits, draft_tokens, temperature)
+        a = PipelineArgs()
+        a.hidden, a.w, a.head_dtype = hidden.data_ptr(), w.data_ptr(), _dtype_code(hidden)
+        a.bias, a.H, a.verify_ms, a.n_max, a.mode = float(bias), hidden.shape[2], verify_ms.data_ptr(), \
+            verify_ms.numel() - 1, int(mode)
+        a.rule, a.B, a.V, a.kmax = int(rule), B, V, kmax
+        a.draft_logits, a.draft_dtype = draft_logits.data_ptr(), _dtype_code(draft_logits)
+        a.target_logits, a.target_dtype = target_logits.data_ptr(), _dtype_code(target_logits)
+        a.draft_tokens, a.temperature = draft_tokens.data_ptr(), temperature.data_ptr()
+        a.seed, a.step = int(seed) & 0xFFFFFFFFFFFFFFFF, self.step.data_ptr()
+        o = self.out
+        a.c_out, a.a_out, a.k_out, a.cu_drafts_out = (o[k].data_ptr() for k in ("c", "a", "k", "cu"))
+        a.accepted_len, a.out_tokens, a.n_emitted, a.status = (
+            o[k].data_ptr() for k in ("accepted_len", "out_tokens", "n_emitted", "status"))
+        a.diag = o["diag"].data_ptr() if diag else None
+        a.accept_counts = self.counts.data_ptr() if counters else None
+        a.workspace, a.workspace_bytes = self.workspace.data_ptr(), self.workspace.numel()
+        self._handle = ctypes.c_void_p()
+        _check(lib().spec_pipeline_create(ctypes.byref(a), ctypes.byref(self._handle)))
+
+    def launch(self, stream=None):
+        """One verify step (one graph launch on the current or given stream)."""
+        _check(lib().spec_pipeline_launch(self._handle, _stream(stream)))
+        return self.out
+
+    def close(self):
+        if self._handle:
+            _check(lib().spec_pipeline_destroy(self._handle))
+            self._handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def spec_verify_workspace_bytes(B, kmax):

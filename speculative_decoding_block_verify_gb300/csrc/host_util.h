@@ -34,4 +34,9 @@ inline int set_cuda_error(cudaError_t e, const char* where) {
 
 inline bool valid_dtype(int d) { return d == SPEC_DTYPE_F32 || d == SPEC_DTYPE_BF16; }
 
+// The verify over the dense [B, kmax (+1), V] layout with the step read from device memory
+// (defined in verify.cu; used by the adaptive pipeline).
+int verify_dense_launch(int rule, const spec_verify_args* a, const uint64_t* step_dev, void* stream,
+                        bool prepare_only);
+
 }  // namespace sv

@@ -69,7 +69,21 @@ struct VerifyParams {
     int64_t stats_warps; // warps of the stats grid
     char* ws;            // workspace (layout below)
     char* list;          // the sweep's work list: the end of the workspace the caller passed
+    int32_t dense;       // 1: logits and tokens in the dense [B, kmax (+1)] layout (see below)
+    const uint64_t* step_dev;   // non-null: the Philox step is read from here (graph replays)
 };
+
+// Logit rows of (stream b, slot i).  Packed layout (the public verify calls): draft row
+// cu[b] + i, target row cu[b] + b + i.  Dense layout (the adaptive pipeline, where the drafter
+// always fills kmax slots and the controller picks how many are verified): draft row
+// b kmax + i, target row b (kmax + 1) + i; draft tokens follow the draft rows.
+__device__ __forceinline__ int64_t qrow_of(const VerifyParams& p, int b, int base, int i) {
+    return p.dense ? (int64_t)b * p.kmax + i : (int64_t)base + i;
+}
+__device__ __forceinline__ int64_t prow_of(const VerifyParams& p, int b, int base, int i) {
+    return p.dense ? (int64_t)b * (p.kmax + 1) + i : (int64_t)base + b + i;
+}
+__device__ __forceinline__ uint64_t step_of(const VerifyParams& p) { return p.step_dev ? *p.step_dev : p.step; }
 
 // Per-piece partial of one row.  T > 0: K = integer reference, (s_hi, s_lo) = sum 2^(l a - K).
 // T = 0: K = the piece maximum, idx = its lowest index.
@@ -857,10 +871,10 @@ __global__ void __launch_bounds__(kStatsThreads, 768 / kStatsThreads) stats_kern
         char* blk = row_block(p, rho);
         Part* dst = blk_at<Part>(blk, kOffParts) + slot;
         if (draft)
-            stats_piece<DQ, E>(ring, row_ptr<DQ>(p.dq, (int64_t)p.cu[b] + (j - Nb - 1), V), c, c_end, false, ah, al,
+            stats_piece<DQ, E>(ring, row_ptr<DQ>(p.dq, qrow_of(p, b, p.cu[b], (int)(j - Nb - 1)), V), c, c_end, false, ah, al,
                                lane, dst, after_last);
         else
-            stats_piece<DP, E>(ring, row_ptr<DP>(p.dp, (int64_t)p.cu[b] + b + j, V), c, c_end, greedy, ah, al, lane,
+            stats_piece<DP, E>(ring, row_ptr<DP>(p.dp, prow_of(p, b, p.cu[b], (int)j), V), c, c_end, greedy, ah, al, lane,
                                dst, after_last);
         if (lane == 0) atomicAdd(blk_at<unsigned>(blk, kOffStatsCount), 1u);   // after lane 0's partial
     };
@@ -961,7 +975,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const VerifyParams p) 
     const bool greedy = (T == 0.f);
     const df a = (temp_ok && !greedy) ? scale_of_temperature(T) : df{0.f, 0.f};
     if (tid <= p.kmax && temp_ok && !greedy) {
-        const uint4 c = make_uint4((uint32_t)tid, (uint32_t)b, (uint32_t)p.step, (uint32_t)(p.step >> 32));
+        const uint64_t stp = step_of(p);
+        const uint4 c = make_uint4((uint32_t)tid, (uint32_t)b, (uint32_t)stp, (uint32_t)(stp >> 32));
         const uint4 wds = philox4x32_10(c, make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
         sh.u_acc[tid] = uniform24_df(wds.x);
     }
@@ -975,12 +990,12 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const VerifyParams p) 
     const int64_t V = p.V;
     bool bad_tok = false;
     if (offsets_ok && temp_ok && tid < N) {
-        const int xi = p.tokens[base + tid];
+        const int xi = p.tokens[qrow_of(p, b, base, tid)];
         sh.x[tid] = xi;
         bad_tok = (xi < 0 || xi >= p.V);
         if (!bad_tok && !greedy) {
-            sh.lq[tid] = load_elem<DQ>(row_ptr<DQ>(p.dq, (int64_t)base + tid, V), xi);
-            sh.lp[tid] = load_elem<DP>(row_ptr<DP>(p.dp, (int64_t)base + b + tid, V), xi);
+            sh.lq[tid] = load_elem<DQ>(row_ptr<DQ>(p.dq, qrow_of(p, b, base, tid), V), xi);
+            sh.lp[tid] = load_elem<DP>(row_ptr<DP>(p.dp, prow_of(p, b, base, tid), V), xi);
         }
     }
     bad_tok = __syncthreads_or(bad_tok);
@@ -1408,8 +1423,8 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const VerifyParams p
         unsigned long long nxt = total;
         int nword = 0;
         const int64_t gb = 2 * (int64_t)p.cu[b] + b;
-        const void* rq = bonus ? nullptr : row_ptr<DQ>(p.dq, (int64_t)p.cu[b] + i, V);
-        const void* rp = row_ptr<DP>(p.dp, (int64_t)p.cu[b] + b + i, V);
+        const void* rq = bonus ? nullptr : row_ptr<DQ>(p.dq, qrow_of(p, b, p.cu[b], i), V);
+        const void* rp = row_ptr<DP>(p.dp, prow_of(p, b, p.cu[b], i), V);
         const int s1 = min(p.nseg, s0 + kSegsPerClaim);
         // once this claim's last copy is issued: the next claim's entry is loaded while the
         // rest of this one is summed
@@ -1466,7 +1481,8 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) 
     const int64_t ob = (int64_t)b * (p.kmax + 1);
     // ---- prologue (inputs only): the per-slot uniforms and the stream's offsets
     if (tid <= p.kmax) {
-        const uint4 c = make_uint4((uint32_t)tid, (uint32_t)b, (uint32_t)p.step, (uint32_t)(p.step >> 32));
+        const uint64_t stp = step_of(p);
+        const uint4 c = make_uint4((uint32_t)tid, (uint32_t)b, (uint32_t)stp, (uint32_t)(stp >> 32));
         const uint4 wds = philox4x32_10(c, make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
         sh.u_acc[tid] = uniform24_df(wds.x);
         sh.u_smp[tid] = wds.y;
@@ -1554,8 +1570,8 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) 
     const float ah = sh.a_hi, al = sh.a_lo;
     const df one{1.f, 0.f};
     const bool block = (p.rule == 1);
-    auto qrow = [&](int i) { return row_ptr<DQ>(p.dq, (int64_t)base + i, V); };
-    auto prow = [&](int i) { return row_ptr<DP>(p.dp, (int64_t)base + b + i, V); };
+    auto qrow = [&](int i) { return row_ptr<DQ>(p.dq, qrow_of(p, b, base, i), V); };
+    auto prow = [&](int i) { return row_ptr<DP>(p.dp, prow_of(p, b, base, i), V); };
 
     if (sh.status == SPEC_ST_OK && !greedy && sh.n_pass > 0) {
         const int np = sh.n_pass;
@@ -1711,7 +1727,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) 
         const float qnan = __int_as_float(0x7fffffff);
         const float ln2 = 0.6931471805599453f;
         const bool have = (!greedy) && (st == SPEC_ST_OK || st == SPEC_ST_NUMERIC);
-        const int64_t tbase = (int64_t)base + b;
+        const int64_t tbase = prow_of(p, b, base, 0);
         for (int i = tid; i <= N; i += kThreads) {
             float* d = p.diag + (tbase + i) * SPEC_DIAG_COLS;
             float v[SPEC_DIAG_COLS];
@@ -1901,6 +1917,8 @@ static int verify_entry(const spec_verify_args* a, void* stream, int rule, const
     p.n_emit = a->n_emitted;
     p.status = a->status;
     p.diag = a->diag;
+    p.dense = 0;
+    p.step_dev = nullptr;
     const bool aligned = (a->V % 8 == 0) && ((uintptr_t)a->target_logits % 16 == 0) &&
                          ((uintptr_t)a->draft_logits % 16 == 0);
     p.nchunk = aligned ? a->V / 8 : a->V;
@@ -1920,6 +1938,55 @@ static int verify_entry(const spec_verify_args* a, void* stream, int rule, const
     if (e != cudaSuccess) return set_cuda_error(e, name);
     if (info) info[2] = aligned ? 8 : 1;
     return clear_error();
+}
+
+// The verify over the dense layout (draft row b kmax + i, target row b (kmax + 1) + i, N_b =
+// cu[b + 1] - cu[b] of them used), the Philox step read from device memory: the adaptive
+// pipeline's verify, whose counts come from the controller on the device.  `prepare_only`
+// sets the kernels' attributes and grid sizes and launches nothing (before a graph capture).
+int verify_dense_launch(int rule, const spec_verify_args* a, const uint64_t* step_dev, void* stream,
+                        bool prepare_only) {
+    const char* name = "spec_pipeline (verify)";
+    int rc = check_args(a, name, !prepare_only);
+    if (rc != SPEC_OK) return rc;
+    VerifyParams p;
+    p.B = a->B;
+    p.V = a->V;
+    p.kmax = a->kmax;
+    p.rule = rule;
+    p.cu = a->cu_drafts;
+    p.dq = a->draft_logits;
+    p.dp = a->target_logits;
+    p.tokens = a->draft_tokens;
+    p.temp = a->temperature;
+    p.seed = a->seed;
+    p.step = 0;
+    p.acc_len = a->accepted_len;
+    p.out_tok = a->out_tokens;
+    p.n_emit = a->n_emitted;
+    p.status = a->status;
+    p.diag = a->diag;
+    p.dense = 1;
+    p.step_dev = step_dev;
+    const bool aligned = (a->V % 8 == 0) && ((uintptr_t)a->target_logits % 16 == 0) &&
+                         ((uintptr_t)a->draft_logits % 16 == 0);
+    p.nchunk = aligned ? a->V / 8 : a->V;
+    p.seg_chunks = (p.nchunk + kSegs - 1) / kSegs;
+    p.nseg = (int32_t)((p.nchunk + p.seg_chunks - 1) / p.seg_chunks);
+    p.ws = reinterpret_cast<char*>(a->workspace);
+    if (!prepare_only) {
+        const size_t need = workspace_bytes(a->B, a->kmax);
+        if (a->workspace == nullptr || a->workspace_bytes < need || (uintptr_t)a->workspace % 16 != 0)
+            return set_error(SPEC_ERR_WORKSPACE, "%s: workspace needs %zu bytes, 16-byte aligned (got %zu)", name,
+                             need, a->workspace_bytes);
+        p.list = p.ws + ((a->workspace_bytes - work_list_claims(a->B, a->kmax) * sizeof(SweepItem)) & ~(size_t)15);
+    }
+    int info[3];
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = aligned ? dispatch_dtypes<8>(p, a->draft_dtype, a->target_dtype, s, prepare_only ? info : nullptr)
+                                  : dispatch_dtypes<1>(p, a->draft_dtype, a->target_dtype, s, prepare_only ? info : nullptr);
+    if (e != cudaSuccess) return set_cuda_error(e, name);
+    return SPEC_OK;
 }
 
 }  // namespace sv
