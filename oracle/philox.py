@@ -17,7 +17,9 @@ measured"; the layout below is this library's reading):
   rule, and eta_{slot+1} for block verification (the same number, so the two rules are
   coupled draw for draw);
 * output word 1 -> the sampling uniform used when the step ends at ``slot`` (the correction
-  token at a rejection, or the bonus token at slot N).
+  token at a rejection, or the bonus token at slot N);
+* output word 2 -> the draft-side uniform of slot ``slot``: the Markov walk samples the draft
+  token t_slot with it (a word the verify does not use, so the two draws are independent).
 * U(x) = ((x >> 8) + 0.5) * 2**-24: 24 random bits, strictly inside (0, 1), exact in float64.
 """
 
@@ -89,6 +91,11 @@ def slot_uniforms(seed, step, stream, slot):
     """(acceptance uniform, sampling uniform) of one (stream, slot) in one verify step."""
     w = philox4x32_10(_counter(step, stream, slot), _key(seed))
     return uniform24(w[0]), uniform24(w[1])
+
+
+def draft_uniform(seed, step, stream, slot):
+    """The draft-side uniform (word 2) of one (stream, slot) in one step."""
+    return uniform24(philox4x32_10(_counter(step, stream, slot), _key(seed))[2])
 
 
 def slot_uniforms_np(seed, step, stream, slot):
