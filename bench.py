@@ -497,7 +497,21 @@ def secondary(sv, workloads, torch, dev):
                                      "bias_GBps_cold_W2": w2_bytes / (ms_cold / 1e3) / 1e9,
                                      "pipeline_us_per_step": ms_pipe * 1e3,
                                      "slots_per_s": 5 / (ms_pipe / 1e3)}
-    del scrub
+    # the same stream with the draft tokens sampled by the Markov walk (slot i biased by t_{i-1})
+    anchor = prev[:1].contiguous()
+    wo = sv.dspark_markov_walk(dq.view(1, 5, -1), anchor, w1, w2, T, 0, 0)
+
+    def walk_only(i):
+        sv.dspark_markov_walk(dq.view(1, 5, -1), anchor, w1, w2, T, 0, i, out=wo)
+    ms_walk = _time(walk_only, 30, stream)
+
+    def walk_then_verify(i):
+        sv.dspark_markov_walk(dq.view(1, 5, -1), anchor, w1, w2, T, 0, i, out=wo)
+        sv.spec_verify_block(cu, wo["logits"].view(5, -1), dp, wo["tokens"].view(-1), T, 5, 0, i)
+    ms_wv = _time(walk_then_verify, 30, stream)
+    res["single_walk_then_block"] = {"walk_us": ms_walk * 1e3, "pipeline_us_per_step": ms_wv * 1e3,
+                                     "slots_per_s": 5 / (ms_wv / 1e3)}
+    del scrub, wo
     # adaptive: pick k (B=128, H=7168) then ragged block verify
     c = workloads.make_confidence_inputs(12)
     h = torch.as_tensor(c["hidden"], device=dev).to(torch.bfloat16)

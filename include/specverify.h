@@ -3,6 +3,8 @@
  *
  * Four calls make up the hot path of one DSpark verify step:
  *   dspark_markov_bias     - the Markov head's low-rank previous-token logit bias
+ *                            (dspark_markov_walk: the same bias with the draft tokens sampled
+ *                            slot by slot)
  *   spec_verify_tokenwise  - token-by-token speculative sampling
  *   spec_verify_block      - block verification
  *   adaptive_pick_k        - confidence head + the controller that picks how many drafts to verify
@@ -105,6 +107,35 @@ extern "C" {
 int dspark_markov_bias(const void* draft_logits, int32_t draft_dtype, int32_t rows, int32_t V,
                        const int32_t* prev_tokens, const void* W1, const void* W2,
                        int32_t w_dtype, int32_t rank, float* out_logits, void* stream);
+
+/*
+ * dspark_markov_walk - the draft-side Markov walk: bias slot i by the token sampled at slot
+ * i - 1, then sample t_i, left to right ([P1] §3 "The Markov fix-up" and Figure 2; [P2] §6):
+ *
+ *   l~_i = l_i + W1[t_{i-1}] @ W2   (t_{-1} = anchor[b]),   t_i ~ softmax(l~_i / T_b)
+ *
+ * The draw is the verify calls' inverse CDF with the draft-side uniform: word 2 of the Philox
+ * output for (slot i, stream b, step) under `seed` (the verify uses words 0 and 1 of the same
+ * counter, so the two draws are independent); T_b = 0 takes the argmax (lowest index).
+ * draft_logits [B, N, V] (draft_dtype) are the drafter's unbiased slot logits; W1 [V, rank],
+ * W2 [rank, V] (w_dtype); anchor [B] int32; temperature [B] float.  Outputs: out_tokens
+ * [B, N] int32 (the draft tokens; -1 from a slot a stream could not sample on), out_logits
+ * [B, N, V] float32 (the biased rows: the draft logits a verify call takes), status [B]:
+ * SPEC_ST_OK, BAD_TEMPERATURE, BAD_TOKEN (anchor outside [0, V)), BAD_ROW (a biased row with
+ * NaN, +inf or no finite entry; the stream stops there), TIMEOUT (a bounded grid wait gave up).
+ * workspace: dspark_markov_walk_workspace_bytes(B) bytes of device scratch, 16-byte aligned,
+ * any contents (the call clears what it needs).  One cooperative launch: N slots for every
+ * group of four streams, two grid-wide barriers per slot.
+ * Errors: SPEC_ERR_ARG (NULL pointer), SPEC_ERR_DTYPE, SPEC_ERR_SHAPE (B < 0, N outside
+ * [0, SPEC_MAX_KMAX], V outside [1, SPEC_MAX_V], rank outside [1, 1024]), SPEC_ERR_WORKSPACE,
+ * SPEC_ERR_CUDA.  B == 0 launches nothing.
+ */
+int dspark_markov_walk(const void* draft_logits, int32_t draft_dtype, int32_t B, int32_t N, int32_t V,
+                       const int32_t* anchor, const void* W1, const void* W2, int32_t w_dtype, int32_t rank,
+                       const float* temperature, uint64_t seed, uint64_t step, int32_t* out_tokens,
+                       float* out_logits, int32_t* status, void* workspace, size_t workspace_bytes,
+                       void* stream);
+size_t dspark_markov_walk_workspace_bytes(int32_t B);
 
 /*
  * Arguments shared by both verify calls.  B streams; stream b has

@@ -8,6 +8,7 @@ kernels; there is no fallback.  PyTorch supplies device memory and streams.
 Entry points (same names as the C ABI):
 
 * ``dspark_markov_bias``     - Markov head's low-rank previous-token logit bias
+* ``dspark_markov_walk``     - the bias with the draft tokens sampled slot by slot
 * ``spec_verify_tokenwise``  - token-by-token speculative sampling
 * ``spec_verify_block``      - block verification
 * ``adaptive_pick_k``        - confidence head + pick how many drafts to verify
@@ -23,8 +24,8 @@ import ctypes
 import os
 
 __all__ = [
-    "dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block", "adaptive_pick_k",
-    "spec_accept_counters", "acceptance_rates", "SpecPipeline",
+    "dspark_markov_bias", "dspark_markov_walk", "spec_verify_tokenwise", "spec_verify_block",
+    "adaptive_pick_k", "spec_accept_counters", "acceptance_rates", "SpecPipeline",
     "spec_philox_uniforms", "spec_verify_launch_info",
     "spec_verify_workspace_bytes", "spec_verify_block_static", "lib", "lib_path", "SpecError",
     "DTYPE_F32", "DTYPE_BF16", "STATUS_NAMES", "DIAG_COLS",
@@ -35,7 +36,8 @@ DTYPE_BF16 = 1
 DIAG_COLS = 8
 STATUS_NAMES = {0: "OK", 1: "BAD_TEMPERATURE", 2: "BAD_TOKEN", 3: "BAD_ROW",
                 4: "ZERO_DRAFT_PROB", 5: "BAD_OFFSETS", 6: "TIMEOUT", 7: "NUMERIC"}
-EXPORTED = ["dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block",
+EXPORTED = ["dspark_markov_bias", "dspark_markov_walk", "dspark_markov_walk_workspace_bytes",
+            "spec_verify_tokenwise", "spec_verify_block",
             "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info",
             "spec_verify_workspace_bytes", "spec_verify_block_static",
             "spec_accept_counters", "spec_pipeline_create", "spec_pipeline_launch",
@@ -104,6 +106,10 @@ def lib():
     L = ctypes.CDLL(path)
     vp, i32, u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64
     L.dspark_markov_bias.argtypes = [vp, i32, i32, i32, vp, vp, vp, i32, i32, vp, vp]
+    L.dspark_markov_walk.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, i32, i32, vp, u64, u64, vp, vp, vp, vp,
+                                     ctypes.c_size_t, vp]
+    L.dspark_markov_walk_workspace_bytes.argtypes = [i32]
+    L.dspark_markov_walk_workspace_bytes.restype = ctypes.c_size_t
     L.spec_verify_tokenwise.argtypes = [ctypes.POINTER(VerifyArgs), vp]
     L.spec_verify_block.argtypes = [ctypes.POINTER(VerifyArgs), vp]
     L.spec_verify_block_static.argtypes = [ctypes.POINTER(VerifyArgs), vp]
@@ -120,7 +126,7 @@ def lib():
     L.spec_verify_workspace_bytes.restype = ctypes.c_size_t
     L.spec_last_error.restype = ctypes.c_char_p
     L.spec_version.restype = ctypes.c_int32
-    for name in ("dspark_markov_bias", "spec_verify_tokenwise", "spec_verify_block", "spec_verify_block_static",
+    for name in ("dspark_markov_bias", "dspark_markov_walk", "spec_verify_tokenwise", "spec_verify_block", "spec_verify_block_static",
                  "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info",
                  "spec_accept_counters", "spec_pipeline_create", "spec_pipeline_launch",
                  "spec_pipeline_destroy"):
@@ -192,6 +198,37 @@ def dspark_markov_bias(draft_logits, prev_tokens, W1, W2, out=None, stream=None)
     _check(lib().dspark_markov_bias(_ptr(draft_logits), _dtype_code(draft_logits), rows, V,
                                     _ptr(prev_tokens), _ptr(W1), _ptr(W2), _dtype_code(W1), R,
                                     _ptr(out), _stream(stream)))
+    return out
+
+
+def dspark_markov_walk(draft_logits, anchor, W1, W2, temperature, seed, step, out=None, stream=None):
+    """The Markov walk: draft_logits [B, N, V] (float32/bf16), anchor [B] int32, W1 [V, R], W2
+    [R, V] (one dtype), temperature [B] float32.  Returns (and reuses) ``out`` with tokens
+    [B, N] int32, logits [B, N, V] float32 (the biased rows), status [B] int32, workspace."""
+    torch = _torch()
+    _dev(draft_logits, "draft_logits")
+    _dev(anchor, "anchor", torch.int32)
+    _dev(W1, "W1")
+    _dev(W2, "W2")
+    _dev(temperature, "temperature", torch.float32)
+    B, N, V = draft_logits.shape
+    R = W2.shape[0]
+    if W1.dtype != W2.dtype or tuple(W1.shape) != (V, R) or tuple(W2.shape) != (R, V):
+        raise ValueError("W1 must be [V, R] and W2 [R, V] with one dtype")
+    if anchor.shape != (B,) or temperature.shape != (B,):
+        raise ValueError("anchor and temperature must be [B]")
+    dev = draft_logits.device
+    if out is None:
+        out = {"tokens": torch.empty((B, N), dtype=torch.int32, device=dev),
+               "logits": torch.empty((B, N, V), dtype=torch.float32, device=dev),
+               "status": torch.empty(B, dtype=torch.int32, device=dev),
+               "workspace": torch.empty(max(int(lib().dspark_markov_walk_workspace_bytes(B)), 16),
+                                        dtype=torch.uint8, device=dev)}
+    _check(lib().dspark_markov_walk(_ptr(draft_logits), _dtype_code(draft_logits), B, N, V, _ptr(anchor),
+                                    _ptr(W1), _ptr(W2), _dtype_code(W1), R, _ptr(temperature),
+                                    int(seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF,
+                                    _ptr(out["tokens"]), _ptr(out["logits"]), _ptr(out["status"]),
+                                    _ptr(out["workspace"]), out["workspace"].numel(), _stream(stream)))
     return out
 
 

@@ -158,6 +158,33 @@ struct Chunk<float, 1> {
     __device__ __forceinline__ void unpack(float (&x)[1]) const { x[0] = v; }
 };
 
+// float32 rows written earlier by the same kernel (other CTAs, or the read-only path's cache
+// from an earlier step): loaded through L2 (ld.global.cg), never through the read-only path.
+struct f32_coherent {
+    float v;
+};
+template <>
+struct Chunk<f32_coherent, 8> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const void* row, int64_t chunk) {
+        const float4* p = reinterpret_cast<const float4*>(row) + 2 * chunk;
+        a = __ldcg(p);
+        b = __ldcg(p + 1);
+    }
+    __device__ __forceinline__ void unpack(float (&x)[8]) const {
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+};
+template <>
+struct Chunk<f32_coherent, 1> {
+    float v;
+    __device__ __forceinline__ void load(const void* row, int64_t chunk) {
+        v = __ldcg(reinterpret_cast<const float*>(row) + chunk);
+    }
+    __device__ __forceinline__ void unpack(float (&x)[1]) const { x[0] = v; }
+};
+
 // One element of a row (any alignment).
 template <typename T>
 __device__ __forceinline__ float load_elem(const void* row, int64_t i);
