@@ -545,11 +545,32 @@ def secondary(sv, workloads, torch, dev):
                          dn["draft_tokens"].view(B, K), dn["temperature"], rule=1)
     ms_graph = _time(lambda i: pl.launch(), 30, stream)
     a_p, marg, tps = sv.acceptance_rates(pl.counts, K)
+    # the same graph with the online cost curve in the loop (P3): an event pair around every
+    # step filed under B + cu_drafts_out[B] tokens, folded in without waiting, the rebuilt
+    # table uploaded into the verify_ms the graph reads
+    curve = sv.CostCurve(c["verify_ms"])
+
+    def step_with_curve(i):
+        curve.begin()
+        pl.launch()
+        curve.end(B, device_count=pl.out["cu"][B:B + 1])
+        curve.poll()
+        curve.upload(vm)
+    ms_curve = _time(step_with_curve, 64, stream)
+    torch.cuda.synchronize()
+    curve.poll()
+    table, cc = curve.table()
+    n_tok = B + int(pl.out["cu"][B].item())
     res["adaptive128_graph"] = {
         "graph_us_per_step": ms_graph * 1e3,
         "eager_us_per_step": ms_ad * 1e3,
+        "with_online_cost_curve_us_per_step": ms_curve * 1e3,
+        "cost_curve": {"observations": cc["observations"], "rebuilds": cc["rebuilds"],
+                       "tokens_last_step": n_tok, "boot_ms": float(c["verify_ms"][n_tok]),
+                       "learned_ms": table[n_tok]},
         "drafts_verified_per_step": int(pl.out["k"].sum().item()),
         "a_p": a_p, "tokens_per_step": tps}
+    curve.close()
     pl.close()
     del dn, pl
     torch.cuda.empty_cache()

@@ -17,7 +17,10 @@
  * Conventions shared by every call
  *   - Every tensor argument is a DEVICE pointer to caller-owned memory, row-major and dense.
  *     The library never allocates, never frees and never keeps a pointer after the call
- *     returns.  It keeps no state between calls.
+ *     returns.  It keeps no state between calls.  Two handles are the exceptions, each
+ *     owning what it creates until its destroy call: the adaptive pipeline (a CUDA graph
+ *     that keeps the device pointers it was created with) and the online cost curve (host
+ *     memory, CUDA events and two pinned buffers).
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
  *     stream) and never synchronises the host.  Outputs are valid once the stream reaches
  *     the end of the call's work.  Calls on the same stream are ordered.
@@ -34,7 +37,8 @@
  *   - Random numbers: Philox4x32-10 (Salmon et al., SC'11), key = (seed lo, seed hi),
  *     counter = (slot, stream, step lo, step hi).  Output word 0 is the acceptance uniform
  *     of draft slot `slot` (u_slot for the token-wise rule, eta_{slot+1} for block
- *     verification); word 1 is the sampling uniform used when the step ends at `slot`.
+ *     verification); word 1 is the sampling uniform used when the step ends at `slot`; word 2
+ *     is the draft-side uniform of slot `slot` (dspark_markov_walk).
  *     U(x) = ((x >> 8) + 0.5) * 2^-24.  Same (seed, step) => bit-identical outputs.
  */
 #ifndef SPECVERIFY_H
@@ -353,6 +357,51 @@ int spec_pipeline_create(const spec_pipeline_args* args, void** pipeline);
 int spec_pipeline_launch(void* pipeline, void* stream);
 /* Release the graph (NULL is accepted). */
 int spec_pipeline_destroy(void* pipeline);
+
+/*
+ * The online verify-cost curve (host code; the table adaptive_pick_k reads).
+ * [P3] "What we changed": a pair of CUDA events is recorded around every real verification
+ * step; the elapsed time is read later without making the host wait, and filed under the
+ * step's token count (the tokens in the verify pass); every rebuild_every observations the
+ * table is rebuilt from the boot curve with the median of the last `window` observations of
+ * every count that has at least min_samples of them laid on top ([P3] "Reproduce": window
+ * 32, min samples 3, rebuild every 32).  The median of an even number of samples is the
+ * mean of the two middle ones.  A curve belongs to one host thread at a time.
+ *
+ * spec_cost_curve_create: boot_ms [n_max + 1] host floats (copied; index = token count).
+ *   Returns an opaque handle, or NULL (spec_last_error says why: boot_ms NULL, n_max < 1,
+ *   window < 1, min_samples outside [1, window], rebuild_every < 1).  Touches no device.
+ * spec_cost_curve_begin / spec_cost_curve_end: bracket one verification step on `stream`
+ *   (a stream that is not being captured: SPEC_ERR_ARG otherwise).  The step's token count is
+ *   num_tokens, plus *device_count when device_count is not NULL (e.g. cu_drafts_out[B] of
+ *   adaptive_pick_k, with num_tokens = B for the bonus rows); that int32 is read back with a
+ *   4-byte copy queued after the end event, outside the timed region.  When 64 steps are
+ *   still pending the step goes unobserved (counted as dropped).  Unmatched begin/end:
+ *   SPEC_ERR_ARG.
+ * spec_cost_curve_poll: folds every completed step, oldest first, into the windows; never
+ *   waits (a step still running stays pending).  Steps whose count falls outside [0, n_max]
+ *   are dropped.
+ * spec_cost_curve_observe: files one observation directly (host clocks, tests); touches no
+ *   device.
+ * spec_cost_curve_table: out [n_max + 1] host floats = the table as last rebuilt (the boot
+ *   curve until the first rebuild); counters [4] (may be NULL) = observations filed, rebuilds,
+ *   dropped, steps pending.  Touches no device.
+ * spec_cost_curve_upload: when the table changed since the last upload, queues its copy into
+ *   device_table [n_max + 1] floats on `stream` from one of two pinned buffers (a buffer whose
+ *   previous copy is still in flight is not overwritten: the upload is then deferred to the
+ *   next call).  A graph that reads device_table (spec_pipeline_create's verify_ms) sees the
+ *   new table from its next launch on that stream.
+ * spec_cost_curve_destroy: waits for the curve's own pending copies, then frees it (NULL ok).
+ */
+void* spec_cost_curve_create(const float* boot_ms, int32_t n_max, int32_t window, int32_t min_samples,
+                             int32_t rebuild_every);
+int spec_cost_curve_begin(void* curve, void* stream);
+int spec_cost_curve_end(void* curve, int32_t num_tokens, const int32_t* device_count, void* stream);
+int spec_cost_curve_poll(void* curve);
+int spec_cost_curve_observe(void* curve, int32_t num_tokens, float ms);
+int spec_cost_curve_table(void* curve, float* out, int64_t* counters);
+int spec_cost_curve_upload(void* curve, float* device_table, void* stream);
+void spec_cost_curve_destroy(void* curve);
 
 /*
  * spec_philox_uniforms - the verify calls' uniforms, exposed for checking.

@@ -14,6 +14,7 @@ Entry points (same names as the C ABI):
 * ``adaptive_pick_k``        - confidence head + pick how many drafts to verify
 * ``spec_accept_counters``   - per-position acceptance counts (a_p, tokens per step)
 * ``SpecPipeline``           - pick k -> ragged verify -> counters as one CUDA graph
+* ``CostCurve``              - the online verify-cost table adaptive_pick_k reads
 * ``spec_philox_uniforms``   - the verify calls' uniforms (for checking)
 
 Build the library first: ``python -m speculative_decoding_block_verify_gb300.build`` (or
@@ -25,7 +26,7 @@ import os
 
 __all__ = [
     "dspark_markov_bias", "dspark_markov_walk", "spec_verify_tokenwise", "spec_verify_block",
-    "adaptive_pick_k", "spec_accept_counters", "acceptance_rates", "SpecPipeline",
+    "adaptive_pick_k", "spec_accept_counters", "acceptance_rates", "SpecPipeline", "CostCurve",
     "spec_philox_uniforms", "spec_verify_launch_info",
     "spec_verify_workspace_bytes", "spec_verify_block_static", "lib", "lib_path", "SpecError",
     "DTYPE_F32", "DTYPE_BF16", "STATUS_NAMES", "DIAG_COLS",
@@ -41,7 +42,10 @@ EXPORTED = ["dspark_markov_bias", "dspark_markov_walk", "dspark_markov_walk_work
             "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info",
             "spec_verify_workspace_bytes", "spec_verify_block_static",
             "spec_accept_counters", "spec_pipeline_create", "spec_pipeline_launch",
-            "spec_pipeline_destroy", "spec_last_error", "spec_version"]
+            "spec_pipeline_destroy", "spec_cost_curve_create", "spec_cost_curve_begin",
+            "spec_cost_curve_end", "spec_cost_curve_poll", "spec_cost_curve_observe",
+            "spec_cost_curve_table", "spec_cost_curve_upload", "spec_cost_curve_destroy",
+            "spec_last_error", "spec_version"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -122,6 +126,16 @@ def lib():
     L.spec_pipeline_create.argtypes = [ctypes.POINTER(PipelineArgs), ctypes.POINTER(vp)]
     L.spec_pipeline_launch.argtypes = [vp, vp]
     L.spec_pipeline_destroy.argtypes = [vp]
+    L.spec_cost_curve_create.argtypes = [vp, i32, i32, i32, i32]
+    L.spec_cost_curve_create.restype = vp
+    L.spec_cost_curve_begin.argtypes = [vp, vp]
+    L.spec_cost_curve_end.argtypes = [vp, i32, vp, vp]
+    L.spec_cost_curve_poll.argtypes = [vp]
+    L.spec_cost_curve_observe.argtypes = [vp, i32, ctypes.c_float]
+    L.spec_cost_curve_table.argtypes = [vp, vp, vp]
+    L.spec_cost_curve_upload.argtypes = [vp, vp, vp]
+    L.spec_cost_curve_destroy.argtypes = [vp]
+    L.spec_cost_curve_destroy.restype = None
     L.spec_verify_workspace_bytes.argtypes = [i32, i32]
     L.spec_verify_workspace_bytes.restype = ctypes.c_size_t
     L.spec_last_error.restype = ctypes.c_char_p
@@ -129,7 +143,9 @@ def lib():
     for name in ("dspark_markov_bias", "dspark_markov_walk", "spec_verify_tokenwise", "spec_verify_block", "spec_verify_block_static",
                  "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info",
                  "spec_accept_counters", "spec_pipeline_create", "spec_pipeline_launch",
-                 "spec_pipeline_destroy"):
+                 "spec_pipeline_destroy", "spec_cost_curve_begin", "spec_cost_curve_end",
+                 "spec_cost_curve_poll", "spec_cost_curve_observe", "spec_cost_curve_table",
+                 "spec_cost_curve_upload"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -436,6 +452,64 @@ class SpecPipeline:
         if self._handle:
             _check(lib().spec_pipeline_destroy(self._handle))
             self._handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class CostCurve:
+    """The online verify-cost curve (P3 "Teaching the Speculator What a Draft Costs", "What we
+    changed" and "Reproduce"): CUDA-event pairs around real verify steps, read without waiting,
+    rolling medians per token count laid over the boot curve every ``rebuild_every``
+    observations.  ``boot_ms`` is a host sequence of n_max + 1 floats (index = token count).
+
+    ``begin()`` / ``end(num_tokens, device_count=None)`` bracket one verify step on the current
+    (or given) stream; a ``device_count`` int32 CUDA tensor (one element) adds its value to the
+    count after the step.  ``poll()`` folds in finished steps, ``table()`` returns the current
+    table (a list) and ``upload(device_table)`` queues its copy into a float32 CUDA tensor."""
+
+    def __init__(self, boot_ms, window=32, min_samples=3, rebuild_every=32):
+        boot = (ctypes.c_float * len(boot_ms))(*[float(v) for v in boot_ms])
+        self.n_max = len(boot_ms) - 1
+        self._handle = lib().spec_cost_curve_create(boot, self.n_max, int(window), int(min_samples),
+                                                     int(rebuild_every))
+        if not self._handle:
+            raise SpecError(-1, lib().spec_last_error().decode())
+
+    def begin(self, stream=None):
+        _check(lib().spec_cost_curve_begin(self._handle, _stream(stream)))
+
+    def end(self, num_tokens=0, device_count=None, stream=None):
+        if device_count is not None:
+            _dev(device_count, "device_count", _torch().int32)
+        _check(lib().spec_cost_curve_end(self._handle, int(num_tokens), _ptr(device_count), _stream(stream)))
+
+    def poll(self):
+        _check(lib().spec_cost_curve_poll(self._handle))
+
+    def observe(self, num_tokens, ms):
+        _check(lib().spec_cost_curve_observe(self._handle, int(num_tokens), float(ms)))
+
+    def table(self):
+        """(table as a list of n_max + 1 floats, {observations, rebuilds, dropped, pending})."""
+        out = (ctypes.c_float * (self.n_max + 1))()
+        cnt = (ctypes.c_int64 * 4)()
+        _check(lib().spec_cost_curve_table(self._handle, out, cnt))
+        return list(out), dict(zip(("observations", "rebuilds", "dropped", "pending"), list(cnt)))
+
+    def upload(self, device_table, stream=None):
+        _dev(device_table, "device_table", _torch().float32)
+        if device_table.numel() != self.n_max + 1:
+            raise ValueError("device_table must hold n_max + 1 floats")
+        _check(lib().spec_cost_curve_upload(self._handle, _ptr(device_table), _stream(stream)))
+
+    def close(self):
+        if self._handle:
+            lib().spec_cost_curve_destroy(self._handle)
+            self._handle = None
 
     def __del__(self):
         try:

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libspecverify.so"
-SOURCES = ["api.cu", "verify.cu", "markov_bias.cu", "pick_k.cu", "pipeline.cu", "walk.cu"]
+SOURCES = ["api.cu", "verify.cu", "markov_bias.cu", "pick_k.cu", "pipeline.cu", "walk.cu", "cost_curve.cu"]
 HEADERS = ["common.cuh", "df.cuh", "draw.cuh", "host_util.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
