@@ -374,8 +374,9 @@ int spec_pipeline_destroy(void* pipeline);
  * spec_cost_curve_begin / spec_cost_curve_end: bracket one verification step on `stream`
  *   (a stream that is not being captured: SPEC_ERR_ARG otherwise).  The step's token count is
  *   num_tokens, plus *device_count when device_count is not NULL (e.g. cu_drafts_out[B] of
- *   adaptive_pick_k, with num_tokens = B for the bonus rows); that int32 is read back with a
- *   4-byte copy queued after the end event, outside the timed region.  When 64 steps are
+ *   adaptive_pick_k, with num_tokens = B for the bonus rows); that int32 is stored into mapped
+ *   pinned memory by a one-thread kernel launched after the end event, outside the timed
+ *   region.  When 64 steps are
  *   still pending the step goes unobserved (counted as dropped).  Unmatched begin/end:
  *   SPEC_ERR_ARG.
  * spec_cost_curve_poll: folds every completed step, oldest first, into the windows; never

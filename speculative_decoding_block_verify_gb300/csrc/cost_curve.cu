@@ -11,8 +11,9 @@
 // in the order they were recorded), and a begin with every pair slot pending records nothing.
 //
 // The token count of a step may live on the device (the controller picks it there): end() then
-// queues a 4-byte read of it into pinned memory after the end event, so the timed region holds
-// the verify alone and the count is read on the host only once that copy has completed.
+// launches a one-thread kernel after the end event that stores it into mapped pinned memory (no
+// copy-engine round trip on the stream), so the timed region holds the verify alone and the
+// count is read on the host only once that store has completed.
 //
 // The table the controller reads lives in device memory; upload() copies the current table
 // there asynchronously on the caller's stream from one of two pinned host buffers, so a copy
@@ -39,7 +40,8 @@ struct CostCurve {
     static constexpr int kPairs = 64;
     cudaEvent_t ev_start[kPairs] = {}, ev_end[kPairs] = {}, ev_ready[kPairs] = {};
     int pair_tokens[kPairs] = {};
-    int32_t* pinned_count = nullptr;           // [kPairs] device counts read back
+    int32_t* pinned_count = nullptr;           // [kPairs] device counts read back (mapped)
+    int32_t* mapped_count = nullptr;           // the device address of pinned_count
     bool from_device[kPairs] = {};
     int head = 0, count = 0;                   // oldest pending pair, pending pairs
     int open = -1;                             // the pair whose end is still to be recorded
@@ -77,6 +79,8 @@ struct CostCurve {
     }
 };
 
+__global__ void read_count_kernel(const int32_t* src, int32_t* dst) { *dst = *src; }
+
 }  // namespace sv
 
 extern "C" void* spec_cost_curve_create(const float* boot_ms, int32_t n_max, int32_t window, int32_t min_samples,
@@ -103,14 +107,21 @@ extern "C" void* spec_cost_curve_create(const float* boot_ms, int32_t n_max, int
 }
 
 static cudaError_t ensure_events(sv::CostCurve* c) {
-    if (c->pinned_count != nullptr) return cudaSuccess;
-    for (int i = 0; i < sv::CostCurve::kPairs; ++i) {
-        cudaError_t e = cudaEventCreate(&c->ev_start[i]);
-        if (e == cudaSuccess) e = cudaEventCreate(&c->ev_end[i]);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_ready[i], cudaEventDisableTiming);
+    if (c->mapped_count != nullptr) return cudaSuccess;
+    for (int i = 0; i < sv::CostCurve::kPairs; ++i) {   // (what a failed earlier call made is kept)
+        cudaError_t e = cudaSuccess;
+        if (c->ev_start[i] == nullptr) e = cudaEventCreate(&c->ev_start[i]);
+        if (e == cudaSuccess && c->ev_end[i] == nullptr) e = cudaEventCreate(&c->ev_end[i]);
+        if (e == cudaSuccess && c->ev_ready[i] == nullptr)
+            e = cudaEventCreateWithFlags(&c->ev_ready[i], cudaEventDisableTiming);
         if (e != cudaSuccess) return e;
     }
-    return cudaMallocHost(reinterpret_cast<void**>(&c->pinned_count), sizeof(int32_t) * sv::CostCurve::kPairs);
+    if (c->pinned_count != nullptr)
+        return cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->mapped_count), c->pinned_count, 0);
+    cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&c->pinned_count), sizeof(int32_t) * sv::CostCurve::kPairs,
+                                  cudaHostAllocMapped);
+    if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->mapped_count), c->pinned_count, 0);
+    return e;
 }
 
 // Event pairs must go on a stream that is not being captured: a captured record is a graph
@@ -155,8 +166,10 @@ extern "C" int spec_cost_curve_end(void* curve, int32_t num_tokens, const int32_
     const int slot = c->open;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaEventRecord(c->ev_end[slot], s);
-    if (e == cudaSuccess && device_count != nullptr)
-        e = cudaMemcpyAsync(c->pinned_count + slot, device_count, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && device_count != nullptr) {
+        sv::read_count_kernel<<<1, 1, 0, s>>>(device_count, c->mapped_count + slot);
+        e = cudaGetLastError();
+    }
     if (e == cudaSuccess) e = cudaEventRecord(c->ev_ready[slot], s);
     if (e != cudaSuccess) return sv::set_cuda_error(e, "spec_cost_curve_end");
     c->pair_tokens[slot] = num_tokens;

@@ -16,6 +16,7 @@
 // in shared memory in the epilogue.  Small CTAs let four of them share an SM, so the ~500
 // column tiles of a 129,280-token vocabulary run as one wave with ~64 KB of W2 in flight per SM.
 
+#include <atomic>
 #include <cfloat>
 
 #include "common.cuh"
@@ -146,14 +147,33 @@ __global__ void __launch_bounds__(kBiasThreads, 4) markov_bias_kernel(const Bias
     }
 }
 
+template <int E>
+constexpr size_t bias_smem_bytes(int R) {
+    return sizeof(float) * ((size_t)kRowGroup * R + (size_t)kBiasWarps * kRowGroup * 32 * E);
+}
+
+// The shared-memory opt-in is set once per device and kernel instance, for the largest rank;
+// later launches skip the driver call.
+template <typename DT, typename WT, int E>
+struct BiasAttr {
+    static std::atomic<int> set[64];
+};
+template <typename DT, typename WT, int E>
+std::atomic<int> BiasAttr<DT, WT, E>::set[64];
+
 template <typename DT, typename WT, int E>
 static cudaError_t launch_bias(const BiasParams& p, cudaStream_t s) {
     constexpr int kTile = 32 * E;
-    const size_t smem = sizeof(float) * ((size_t)kRowGroup * p.R +
-                                         (size_t)kBiasWarps * kRowGroup * kTile);
-    cudaError_t e = cudaFuncSetAttribute(markov_bias_kernel<DT, WT, E>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t smem = bias_smem_bytes<E>(p.R);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !BiasAttr<DT, WT, E>::set[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(markov_bias_kernel<DT, WT, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bias_smem_bytes<E>(kMaxRank));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) BiasAttr<DT, WT, E>::set[dev].store(1, std::memory_order_release);
+    }
     const dim3 grid((unsigned)((p.V + kTile - 1) / kTile),
                     (unsigned)((p.rows + kRowGroup - 1) / kRowGroup));
     markov_bias_kernel<DT, WT, E><<<grid, kBiasThreads, smem, s>>>(p);

@@ -372,9 +372,21 @@ __device__ int valid_prefix(const VerifyParams& p) {
 // ---------------------------------------------------------------------------------------
 // 16-byte rows (E = 8): each warp owns a ring of kStages stages of kStageBytes in shared
 // memory, each filled by one TMA bulk copy (issued by lane 0) that completes on the stage's
-// mbarrier; every lane waits with a bounded poll.
-constexpr int kStages = 4;
-constexpr int kStageBytes = 2048;
+// mbarrier; every lane waits with a bounded poll.  Large stages keep the per-stage work (the
+// wait, the next copy, the reference check) small next to the per-element arithmetic: the
+// scan is bound by issue slots as much as by HBM, about four instructions per logit.
+#ifndef SV_STATS_STAGES
+#define SV_STATS_STAGES 3
+#endif
+#ifndef SV_STATS_STAGE_BYTES
+#define SV_STATS_STAGE_BYTES 4096
+#endif
+#ifndef SV_STATS_MIN_BLOCKS
+#define SV_STATS_MIN_BLOCKS 2
+#endif
+constexpr int kStages = SV_STATS_STAGES;
+constexpr int kStageBytes = SV_STATS_STAGE_BYTES;
+constexpr int kStatsMinBlocks = SV_STATS_MIN_BLOCKS;   // resident CTAs per SM the registers allow
 constexpr int kStatsRingBytes = kStatsWarps * kStages * kStageBytes;
 static size_t stats_smem_bytes(int E) { return E == 8 ? (size_t)kStatsRingBytes : 0; }
 
@@ -415,55 +427,59 @@ __device__ __forceinline__ void stream_piece(const void* row, int64_t c0, int64_
 // The stats kernel's per-warp ring: kStages stages of kStageBytes in shared memory, each
 // filled by one TMA bulk copy (issued by lane 0, with an evict-first L2 policy: the logits are
 // streamed through once and must not push the kernels' code and workspace out of L2) that
-// completes on the stage's mbarrier; every lane waits with a bounded poll.  One instruction per stage moves the data, so the scan's
-// issue slots go to the arithmetic.  Slots and phases persist from piece to piece.
+// completes on the stage's mbarrier; every lane waits with a bounded poll.  Copies are
+// numbered over every piece of the warp: copy q uses slot q mod kStages, and its wait is that
+// slot's (q div kStages)-th completion, so the parity is that count's low bit.
 struct StatsRing {
     char* base;
     uint64_t* bar;
+    uint64_t policy;
+    uint32_t issued, done;   // copies issued / waited for
     int lane;
-    unsigned phase;     // parity of the next completion of each slot
-    unsigned pending;   // slots with a copy issued and not yet waited for
     bool timeout;
     __device__ __forceinline__ void init(char* b, uint64_t* bars, int ln) {
         base = b;
         bar = bars;
         lane = ln;
-        phase = 0;
-        pending = 0;
+        issued = done = 0;
         timeout = false;
+        policy = l2_evict_first_policy();
         if (lane == 0) {
             for (int i = 0; i < kStages; ++i) mbar_init(&bar[i], 1);
             mbar_init_fence();
         }
         __syncwarp();
     }
-    __device__ __forceinline__ void issue(int slot, const char* src, unsigned bytes) {
+    __device__ __forceinline__ void issue(const char* src, unsigned bytes) {
         if (timeout) return;   // after a failed wait nothing new is put in flight
-        pending |= 1u << slot;
+        const uint32_t slot = issued % kStages;
+        ++issued;
         __syncwarp();          // every lane is done with this slot's previous contents
         if (lane == 0) {
             fence_proxy_async_smem();
             mbar_expect_tx(&bar[slot], bytes);
-            bulk_g2s_hint(base + slot * kStageBytes, src, bytes, &bar[slot], l2_evict_first_policy());
+            bulk_g2s_hint(base + slot * kStageBytes, src, bytes, &bar[slot], policy);
         }
     }
-    __device__ __forceinline__ void wait(int slot) {
-        if (timeout) return;
-        const unsigned parity = (phase >> slot) & 1u;
-        int n = 0;
-        while (!mbar_try_wait(&bar[slot], parity)) {
-            if (++n > kSpinLimit) {
-                timeout = true;   // the slot stays pending; drain() waits for it once more
-                return;
+    // Waits for the oldest copy in flight and returns its stage.
+    __device__ __forceinline__ const char* wait() {
+        const uint32_t slot = done % kStages;
+        if (!timeout) {
+            const uint32_t parity = (done / kStages) & 1u;
+            int n = 0;
+            while (!mbar_try_wait(&bar[slot], parity)) {
+                if (++n > kSpinLimit) {
+                    timeout = true;   // this copy stays outstanding; drain() waits for it once more
+                    return base + slot * kStageBytes;
+                }
             }
+            ++done;
         }
-        phase ^= 1u << slot;
-        pending &= ~(1u << slot);
+        return base + slot * kStageBytes;
     }
     __device__ __forceinline__ void drain() {
-        for (int slot = 0; slot < kStages; ++slot) {
-            if (!((pending >> slot) & 1u)) continue;
-            const unsigned parity = (phase >> slot) & 1u;
+        for (uint32_t q = done; q != issued; ++q) {
+            const uint32_t slot = q % kStages, parity = (q / kStages) & 1u;
             for (int n = 0; n < kSpinLimit && !mbar_try_wait(&bar[slot], parity); ++n) {
             }
         }
@@ -472,31 +488,32 @@ struct StatsRing {
 
 // One piece [c0, c1) of a 16-byte aligned row through the bulk ring: full stages go to
 // add_full (U chunks per lane), the ragged last stage chunk by chunk to add.  after_last() runs
-// (in every lane) right after the piece's last copy has been issued, while D - 1 stages are
-// still to be consumed: the next claim is fired there, so its round trip overlaps this tail.
+// (in every lane) right after the piece's last copy has been issued, while kStages - 1 stages
+// are still to be consumed: the next claim is fired there, so its round trip overlaps this tail.
 template <typename T, typename AddFn, typename GroupFn, typename AfterFn>
 __device__ __forceinline__ void stream_piece_bulk(StatsRing& R, const void* row, int64_t c0, int64_t c1, int lane,
                                                   AddFn add, GroupFn add_full, AfterFn after_last) {
     constexpr int BT = 8 * (int)sizeof(T);   // bytes per chunk
     constexpr int G = kStageBytes / BT;      // chunks per stage
     constexpr int U = G / 32;                // chunks per lane and stage
-    const char* g = reinterpret_cast<const char*>(row) + c0 * BT;
+    const char* src = reinterpret_cast<const char*>(row) + c0 * BT;
     const int64_t n = c1 - c0;
     const int nb = (int)((n + G - 1) / G);
-    auto issue = [&](int i) {
-        if (i < nb) {
-            R.issue(i % kStages, g + (int64_t)i * G * BT, (unsigned)(min((int64_t)G, n - (int64_t)i * G) * BT));
-            if (i == nb - 1) after_last();
-        }
+    const int nfull = (int)(n / G);
+    const unsigned last_bytes = (unsigned)((n - (int64_t)(nb - 1) * G) * BT);
+    int next = 0;   // the next stage of the piece to issue
+    auto issue_next = [&]() {
+        R.issue(src, next == nb - 1 ? last_bytes : (unsigned)kStageBytes);
+        src += kStageBytes;
+        if (++next == nb) after_last();
     };
-#pragma unroll
-    for (int i = 0; i < kStages - 1; ++i) issue(i);
-    for (int i = 0; i < nb; ++i) {
-        issue(i + kStages - 1);
-        const int slot = i % kStages;
-        R.wait(slot);
-        const char* st = R.base + slot * kStageBytes;
-        if ((int64_t)(i + 1) * G <= n) {   // a full stage: every lane has all U chunks
+    const int prime = min(nb, kStages - 1);
+    for (int i = 0; i < prime; ++i) issue_next();
+    int64_t k0 = c0 + lane;   // this lane's first chunk of the stage
+    for (int i = 0; i < nb; ++i, k0 += G) {
+        if (next < nb) issue_next();   // into the slot of stage i - 1, consumed
+        const char* st = R.wait();
+        if (i < nfull) {   // a full stage: every lane has all U chunks
             float x[U][8];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -512,7 +529,7 @@ __device__ __forceinline__ void stream_piece_bulk(StatsRing& R, const void* row,
                     x[u][4] = b.x; x[u][5] = b.y; x[u][6] = b.z; x[u][7] = b.w;
                 }
             }
-            add_full(x, c0 + (int64_t)i * G + lane);
+            add_full(x, k0);
         } else {
             const int cnt = (int)(n - (int64_t)i * G);
             for (int kk = lane; kk < cnt; kk += 32) {
@@ -528,7 +545,7 @@ __device__ __forceinline__ void stream_piece_bulk(StatsRing& R, const void* row,
                     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
                     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
                 }
-                add(x, (c0 + (int64_t)i * G + kk) * 8);
+                add(x, (k0 - lane + kk) * 8);
             }
         }
     }
@@ -619,7 +636,7 @@ __device__ __forceinline__ int row_piece_count(int64_t rho, int64_t n, int64_t l
 }
 
 template <typename DQ, typename DP, int E>
-__global__ void __launch_bounds__(kStatsThreads, 768 / kStatsThreads) stats_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) stats_kernel(const VerifyParams p) {
     extern __shared__ __align__(16) char stats_smem[];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ __align__(8) uint64_t stats_bars[kStatsWarps][kStages];
@@ -647,8 +664,10 @@ __global__ void __launch_bounds__(kStatsThreads, 768 / kStatsThreads) stats_kern
     int Nb = p.cu[1] - p.cu[0];
     // one piece [c, c_end) of row rho into partial slot `slot`
     auto piece = [&](int64_t rho, int64_t c, int64_t c_end, int slot, auto after_last) {
-        if (rho > gb + 2 * (int64_t)Nb) {   // rows only move forward for a warp
-            b = stream_of_row(p, rho, b, L);
+        // a warp's static rows only move forward, but its tail claims wrap around from the last
+        // ticket range to the first, so a claimed row may lie before the current stream
+        if (rho < gb || rho > gb + 2 * (int64_t)Nb) {
+            b = stream_of_row(p, rho, rho < gb ? 0 : b, L);
             gb = 2 * (int64_t)p.cu[b] + b;
             Nb = p.cu[b + 1] - p.cu[b];
         }
