@@ -433,3 +433,48 @@ def verify_batch(rule, cu_drafts, draft_logits, target_logits, draft_tokens, tem
             out["diag"][cu[b] + b: cu[b] + b + n + 1] = r["diag"]
             out["gross"][cu[b] + b: cu[b] + b + n + 1] = r["gross"]
     return out
+
+
+# ----------------------------------------------------------------------------------------
+# Reduced draft vocabulary
+# ----------------------------------------------------------------------------------------
+
+class ScatteredRows:
+    """Draft rows scored over a reduced draft vocabulary, seen in target-vocabulary columns.
+
+    P1 "MTP, DSpark and Block Verification, Explained", §3 "The Markov fix-up": the drafter
+    scores a reduced vocabulary and scatters those logits into target-vocabulary columns, so
+    the draft distribution puts no mass outside the reduced vocabulary.  Column v of row r
+    holds reduced[r, t2d[v]] when 0 <= t2d[v] < K and -inf otherwise (t2d is the inverse of
+    the map from draft ids to target columns).  Row-indexable like a [rows, V] array.
+    """
+
+    def __init__(self, reduced, t2d):
+        self.reduced = reduced
+        self.t2d = np.asarray(t2d, np.int64)
+        K = np.asarray(reduced[0]).shape[0] if len(reduced) else 0
+        self.K = K
+        self.inside = (self.t2d >= 0) & (self.t2d < K)
+        ids = self.t2d[self.inside]
+        # every draft id is referenced by exactly one column: the scatter is a bijection
+        # between a reduced row and its columns
+        if len(ids) != K or (K and np.bincount(ids, minlength=K).max() != 1):
+            raise ValueError("t2d must reference every draft id in [0, K) exactly once")
+
+    def __len__(self):
+        return len(self.reduced)
+
+    def __getitem__(self, r):
+        row = np.full(self.t2d.shape[0], -np.inf)
+        row[self.inside] = np.asarray(self.reduced[r], np.float64)[self.t2d[self.inside]]
+        return row
+
+
+def verify_batch_reduced(rule, cu_drafts, reduced_draft_logits, t2d, target_logits, draft_tokens,
+                         temperature, kmax, seed, step, streams=None):
+    """Mirror of spec_verify_tokenwise_reduced / spec_verify_block_reduced: the verify of
+    draft rows given over a reduced draft vocabulary (reduced_draft_logits [cu[B], K], column
+    map t2d [V]), by definition the dense verify of the scattered rows."""
+    return verify_batch(rule, cu_drafts, ScatteredRows(reduced_draft_logits, t2d), target_logits,
+                        draft_tokens, temperature, kmax, seed, step, streams)
+

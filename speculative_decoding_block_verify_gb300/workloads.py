@@ -21,6 +21,13 @@ private transcripts):
 * ``adaptive128``  B=128, kmax=5, H=7168 bf16 hidden ~ N(0, 1); head w ~ N(0, 0.02^2) bf16,
                    beta = 0; verify_ms[n] = 12 + 2.6 n for n = 1..768; ragged verify logits
                    with the batch64 statistics at T = 1 for a given per-stream k.
+* ``batch64_topk`` the batch64 workload with a reduced draft vocabulary of K = 32,768 target
+                   columns (a seeded random subset, in ascending order: d2t [K], and its
+                   inverse t2d [V], -1 outside): the draft rows are [cu[B], K] (the batch64
+                   draft noise on the target logits at those columns), the draft tokens are
+                   target ids sampled over the reduced vocabulary, and the target logits at
+                   the reduced columns are raised by 3 (so that, as for a reduced vocabulary
+                   of frequent tokens, most of the target mass lies inside it).
 
 Draft tokens: for T > 0, x_i is drawn from softmax(draft_i / T) with the Gumbel-max trick
 (argmax of draft_i / T + Gumbel noise) on the *unbiased* draft logits; for T = 0 it is the
@@ -50,7 +57,20 @@ WORKLOADS = {
     "adaptive128": dict(B=128, N=5, V=V_FULL, dtype="bf16", target_std=2.5,
                         noise=("stream_uniform", 0.2, 2.0), temp=("const", 1.0), greedy_frac=0.0,
                         rank=0, H=7168),
+    "batch64_topk": dict(B=64, N=5, V=V_FULL, dtype="bf16", target_std=2.5,
+                         noise=("stream_uniform", 0.2, 2.0), temp=("stream_uniform", 0.3, 1.0),
+                         greedy_frac=0.05, rank=0, draft_vocab=32768, vocab_boost=3.0),
 }
+
+
+def make_draft_vocab(seed, V, K):
+    """A reduced draft vocabulary: d2t [K] (ascending target columns, a seeded random subset)
+    and its inverse t2d [V] (-1 for columns outside it).  Pure layout."""
+    rng = np.random.Generator(np.random.PCG64(seed + 31337))
+    d2t = np.sort(rng.permutation(V)[:K]).astype(np.int32)
+    t2d = np.full(V, -1, np.int32)
+    t2d[d2t] = np.arange(K, dtype=np.int32)
+    return d2t, t2d
 
 
 def round_bf16(a):
@@ -90,7 +110,7 @@ def ragged_cu(k):
     return np.concatenate([[0], np.cumsum(k)]).astype(np.int32)
 
 
-def make_verify_inputs(name, seed, *, B=None, N=None, V=None, k=None, backend="numpy",
+def make_verify_inputs(name, seed, *, B=None, N=None, V=None, k=None, K=None, backend="numpy",
                        device=None):
     """Synthetic verify inputs for workload ``name``.
 
@@ -98,9 +118,12 @@ def make_verify_inputs(name, seed, *, B=None, N=None, V=None, k=None, backend="n
     Returns a dict with numpy arrays (``numpy`` back-end) or torch tensors on ``device``
     (``torch`` back-end): cu_drafts [B+1] int32, draft_logits [cu[B], V] float32,
     target_logits [cu[B]+B, V] float32, draft_tokens [cu[B]] int32, temperature [B]
-    float32, plus B, V, kmax, dtype, name.
+    float32, plus B, V, kmax, dtype, name.  A workload with a reduced draft vocabulary (size
+    K, overridable) returns draft_logits [cu[B], K] instead, plus d2t [K], t2d [V] and K.
     """
     spec = dict(WORKLOADS[name])
+    if "draft_vocab" in spec and K is not None:
+        spec["draft_vocab"] = K
     B = spec["B"] if B is None else B
     V = spec["V"] if V is None else V
     if k is None:
@@ -126,6 +149,12 @@ def _make_numpy(spec, name, seed, B, V, k, cu, kmax):
     n_draft = int(cu[-1])
     n_target = n_draft + B
     target = (rng.standard_normal((n_target, V), dtype=np.float32) * spec["target_std"])
+    reduced = "draft_vocab" in spec
+    if reduced:
+        d2t, t2d = make_draft_vocab(seed, V, spec["draft_vocab"])
+        target[:, d2t] += np.float32(spec["vocab_boost"])
+    cols = d2t if reduced else slice(None)
+    width = len(d2t) if reduced else V
     target = _as_dtype(target, spec["dtype"])
     std = _layout_noise(spec, B, k, lambda lo, hi, n: rng.uniform(lo, hi, n))
     temps = _temps(spec["temp"], B, lambda lo, hi, n: rng.uniform(lo, hi, n))
@@ -134,22 +163,26 @@ def _make_numpy(spec, name, seed, B, V, k, cu, kmax):
     if n_greedy:
         greedy[rng.permutation(B)[:n_greedy]] = True
         temps[greedy] = 0.0
-    draft = np.empty((n_draft, V), np.float32)
+    draft = np.empty((n_draft, width), np.float32)
     tokens = np.empty(n_draft, np.int32)
     for b in range(B):
         for i in range(int(k[b])):
             row = cu[b] + i
-            noise = rng.standard_normal(V, dtype=np.float32) * np.float32(std[b, i])
-            d = _as_dtype(target[cu[b] + b + i] + noise, spec["dtype"])
+            noise = rng.standard_normal(width, dtype=np.float32) * np.float32(std[b, i])
+            d = _as_dtype(target[cu[b] + b + i][cols] + noise, spec["dtype"])
             draft[row] = d
             if greedy[b]:
-                tokens[row] = int(np.argmax(d))
+                j = int(np.argmax(d))
             else:
-                g = -np.log(-np.log(rng.random(V)))
-                tokens[row] = int(np.argmax(d.astype(np.float64) / float(temps[b]) + g))
-    return dict(name=name, B=B, V=V, kmax=kmax, dtype=spec["dtype"], cu_drafts=cu,
-                draft_logits=draft, target_logits=target, draft_tokens=tokens,
-                temperature=temps.astype(np.float32))
+                g = -np.log(-np.log(rng.random(width)))
+                j = int(np.argmax(d.astype(np.float64) / float(temps[b]) + g))
+            tokens[row] = int(d2t[j]) if reduced else j
+    out = dict(name=name, B=B, V=V, kmax=kmax, dtype=spec["dtype"], cu_drafts=cu,
+               draft_logits=draft, target_logits=target, draft_tokens=tokens,
+               temperature=temps.astype(np.float32))
+    if reduced:
+        out.update(d2t=d2t, t2d=t2d, K=len(d2t))
+    return out
 
 
 def _make_torch(spec, name, seed, B, V, k, cu, kmax, device):
@@ -161,7 +194,14 @@ def _make_torch(spec, name, seed, B, V, k, cu, kmax, device):
     n_draft = int(cu[-1])
     n_target = n_draft + B
     tdt = torch.bfloat16 if spec["dtype"] == "bf16" else torch.float32
-    target = (torch.randn((n_target, V), generator=g, device=dev) * spec["target_std"]).to(tdt)
+    target = torch.randn((n_target, V), generator=g, device=dev) * spec["target_std"]
+    reduced = "draft_vocab" in spec
+    if reduced:
+        d2t, t2d = make_draft_vocab(seed, V, spec["draft_vocab"])
+        d2t_dev = torch.as_tensor(d2t.astype(np.int64), device=dev)
+        target[:, d2t_dev] += spec["vocab_boost"]
+    width = len(d2t) if reduced else V
+    target = target.to(tdt)
     std = _layout_noise(spec, B, k, lambda lo, hi, n: host.uniform(lo, hi, n))
     temps = _temps(spec["temp"], B, lambda lo, hi, n: host.uniform(lo, hi, n))
     greedy = np.zeros(B, bool)
@@ -174,26 +214,35 @@ def _make_torch(spec, name, seed, B, V, k, cu, kmax, device):
     row_i = np.concatenate([np.arange(int(n)) for n in k]) if n_draft else np.zeros(0, int)
     trow = torch.as_tensor((cu[row_b] + row_b + row_i).astype(np.int64), device=dev)
     row_std = torch.as_tensor(std[row_b, row_i].astype(np.float32), device=dev)
-    draft = torch.empty((n_draft, V), dtype=tdt, device=dev)
+    draft = torch.empty((n_draft, width), dtype=tdt, device=dev)
     tokens = torch.empty(n_draft, dtype=torch.int32, device=dev)
     row_t = torch.as_tensor(temps[row_b].astype(np.float32), device=dev)
     row_g = torch.as_tensor(greedy[row_b], device=dev)
     chunk = 64
     for r0 in range(0, n_draft, chunk):
         r1 = min(n_draft, r0 + chunk)
-        noise = torch.randn((r1 - r0, V), generator=g, device=dev) * row_std[r0:r1, None]
-        d = (target[trow[r0:r1]].float() + noise).to(tdt)
+        noise = torch.randn((r1 - r0, width), generator=g, device=dev) * row_std[r0:r1, None]
+        base = target[trow[r0:r1]].float()
+        if reduced:
+            base = base[:, d2t_dev]
+        d = (base + noise).to(tdt)
         draft[r0:r1] = d
-        u = torch.rand((r1 - r0, V), generator=g, device=dev, dtype=torch.float64)
+        u = torch.rand((r1 - r0, width), generator=g, device=dev, dtype=torch.float64)
         gum = -torch.log(-torch.log(u))
         t = row_t[r0:r1, None].double().clamp_min(1e-30)
         sampled = torch.argmax(d.double() / t + gum, dim=1)
         greedy_pick = torch.argmax(d.float(), dim=1)
-        tokens[r0:r1] = torch.where(row_g[r0:r1], greedy_pick, sampled).to(torch.int32)
-    return dict(name=name, B=B, V=V, kmax=kmax, dtype=spec["dtype"],
-                cu_drafts=torch.as_tensor(cu, device=dev),
-                draft_logits=draft, target_logits=target, draft_tokens=tokens,
-                temperature=torch.as_tensor(temps.astype(np.float32), device=dev))
+        pick = torch.where(row_g[r0:r1], greedy_pick, sampled)
+        if reduced:
+            pick = d2t_dev[pick]
+        tokens[r0:r1] = pick.to(torch.int32)
+    out = dict(name=name, B=B, V=V, kmax=kmax, dtype=spec["dtype"],
+               cu_drafts=torch.as_tensor(cu, device=dev),
+               draft_logits=draft, target_logits=target, draft_tokens=tokens,
+               temperature=torch.as_tensor(temps.astype(np.float32), device=dev))
+    if reduced:
+        out.update(d2t=torch.as_tensor(d2t, device=dev), t2d=torch.as_tensor(t2d, device=dev), K=len(d2t))
+    return out
 
 
 def make_bias_inputs(name, seed, *, rows=None, V=None, rank=None):
