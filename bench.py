@@ -277,6 +277,8 @@ def algorithmic_bytes(inp):
     V = inp["V"]
     es = 2 if inp["dtype"] == "bf16" else 4
     B = len(cu) - 1
+    if "t2d" in inp:   # reduced draft vocabulary: draft rows of K logits, plus the column map
+        return (int(cu[-1]) + B) * V * es + int(cu[-1]) * inp["K"] * es + V * 4
     rows = 2 * int(cu[-1]) + B
     return rows * V * es
 
@@ -487,6 +489,20 @@ def secondary(sv, workloads, torch, dev):
     res["batch256_k9_fp32_block"] = {"us_per_call": ms * 1e3, "slots_per_s": 2304 / (ms / 1e3),
                                      "GBps": alg / (ms / 1e3) / 1e9}
     del s
+    torch.cuda.empty_cache()
+    # batch-64 block verify with a reduced draft vocabulary (K = 32,768 draft columns)
+    sets = [workloads.make_verify_inputs("batch64_topk", 5100 + i, backend="torch", device=dev) for i in range(3)]
+
+    def red(i):
+        s = sets[i % 3]
+        sv.spec_verify_block_reduced(s["cu_drafts"], s["draft_logits"], s["t2d"], s["target_logits"],
+                                     s["draft_tokens"], s["temperature"], 5, 0, i)
+    ms = _time(red, 50, stream)
+    alg = algorithmic_bytes(sets[0])
+    res["batch64_topk_block"] = {"us_per_call": ms * 1e3, "slots_per_s": 320 / (ms / 1e3),
+                                 "algorithmic_bytes": alg, "GBps": alg / (ms / 1e3) / 1e9,
+                                 "draft_vocab": sets[0]["K"]}
+    del sets
     torch.cuda.empty_cache()
     # single stream: Markov bias (rank 256) then block verify
     inp = workloads.make_verify_inputs("single_bias", 7000)

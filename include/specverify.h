@@ -224,6 +224,26 @@ int spec_verify_tokenwise(const spec_verify_args* args, void* stream);
 int spec_verify_block(const spec_verify_args* args, void* stream);
 
 /*
+ * spec_verify_tokenwise_reduced / spec_verify_block_reduced - the same verify calls with the
+ * draft rows over a reduced draft vocabulary.
+ * [P1] §3 "The Markov fix-up": the drafter scores a reduced vocabulary and scatters those
+ * logits into target-vocabulary columns, so the draft distribution is zero outside it.  The
+ * verify is, by definition, the dense verify of the scattered rows: draft logit of target
+ * column v = draft_logits[row, t2d[v]] when 0 <= t2d[v] < K, and -inf otherwise.
+ * args->draft_logits is [cu_drafts[B], K] (draft_dtype); everything else as in the dense
+ * calls (draft tokens are target-vocabulary ids; one outside the draft vocabulary gives
+ * SPEC_ST_ZERO_DRAFT_PROB at T > 0).  t2d [V] int32 (device): the inverse of the map from draft
+ * ids to target columns - every draft id in [0, K) must appear exactly once (the call does
+ * not check this; with a duplicate or a missing id the result is that of the column-wise
+ * definition above, which is then no distribution scattered from the draft rows).  Only the
+ * target rows are read in full: the draft rows are read once (K logits each) and gathered
+ * through t2d where the residual is summed.  The workspace is that of the dense calls.
+ * Errors: those of the dense calls, SPEC_ERR_ARG (t2d NULL), SPEC_ERR_SHAPE (K outside [1, V]).
+ */
+int spec_verify_tokenwise_reduced(const spec_verify_args* args, const int32_t* t2d, int32_t K, void* stream);
+int spec_verify_block_reduced(const spec_verify_args* args, const int32_t* t2d, int32_t K, void* stream);
+
+/*
  * spec_verify_block_static - spec_verify_block without a caller workspace: the workspace is a
  * fixed device array of 16 MiB (16,777,216 bytes) that the library reserves when it is loaded,
  * so the call allocates no memory at all.  It is for callers that cannot allocate device memory

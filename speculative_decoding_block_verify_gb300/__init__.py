@@ -11,6 +11,7 @@ Entry points (same names as the C ABI):
 * ``dspark_markov_walk``     - the bias with the draft tokens sampled slot by slot
 * ``spec_verify_tokenwise``  - token-by-token speculative sampling
 * ``spec_verify_block``      - block verification
+* ``spec_verify_*_reduced``  - the same over a reduced draft vocabulary (top-k draft columns)
 * ``adaptive_pick_k``        - confidence head + pick how many drafts to verify
 * ``spec_accept_counters``   - per-position acceptance counts (a_p, tokens per step)
 * ``SpecPipeline``           - pick k -> ragged verify -> counters as one CUDA graph
@@ -26,6 +27,7 @@ import os
 
 __all__ = [
     "dspark_markov_bias", "dspark_markov_walk", "spec_verify_tokenwise", "spec_verify_block",
+    "spec_verify_tokenwise_reduced", "spec_verify_block_reduced",
     "adaptive_pick_k", "spec_accept_counters", "acceptance_rates", "SpecPipeline", "CostCurve",
     "spec_philox_uniforms", "spec_verify_launch_info",
     "spec_verify_workspace_bytes", "spec_verify_block_static", "lib", "lib_path", "SpecError",
@@ -39,6 +41,7 @@ STATUS_NAMES = {0: "OK", 1: "BAD_TEMPERATURE", 2: "BAD_TOKEN", 3: "BAD_ROW",
                 4: "ZERO_DRAFT_PROB", 5: "BAD_OFFSETS", 6: "TIMEOUT", 7: "NUMERIC"}
 EXPORTED = ["dspark_markov_bias", "dspark_markov_walk", "dspark_markov_walk_workspace_bytes",
             "spec_verify_tokenwise", "spec_verify_block",
+            "spec_verify_tokenwise_reduced", "spec_verify_block_reduced",
             "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info",
             "spec_verify_workspace_bytes", "spec_verify_block_static",
             "spec_accept_counters", "spec_pipeline_create", "spec_pipeline_launch",
@@ -117,6 +120,8 @@ def lib():
     L.spec_verify_tokenwise.argtypes = [ctypes.POINTER(VerifyArgs), vp]
     L.spec_verify_block.argtypes = [ctypes.POINTER(VerifyArgs), vp]
     L.spec_verify_block_static.argtypes = [ctypes.POINTER(VerifyArgs), vp]
+    L.spec_verify_tokenwise_reduced.argtypes = [ctypes.POINTER(VerifyArgs), vp, i32, vp]
+    L.spec_verify_block_reduced.argtypes = [ctypes.POINTER(VerifyArgs), vp, i32, vp]
     L.adaptive_pick_k.argtypes = [vp, vp, i32, ctypes.c_float, i32, i32, i32, vp, i32, i32,
                                   vp, vp, vp, vp, vp]
     L.spec_philox_uniforms.argtypes = [u64, u64, i32, i32, vp, vp]
@@ -141,6 +146,7 @@ def lib():
     L.spec_last_error.restype = ctypes.c_char_p
     L.spec_version.restype = ctypes.c_int32
     for name in ("dspark_markov_bias", "dspark_markov_walk", "spec_verify_tokenwise", "spec_verify_block", "spec_verify_block_static",
+                 "spec_verify_tokenwise_reduced", "spec_verify_block_reduced",
                  "adaptive_pick_k", "spec_philox_uniforms", "spec_verify_launch_info",
                  "spec_accept_counters", "spec_pipeline_create", "spec_pipeline_launch",
                  "spec_pipeline_destroy", "spec_cost_curve_begin", "spec_cost_curve_end",
@@ -249,7 +255,7 @@ def dspark_markov_walk(draft_logits, anchor, W1, W2, temperature, seed, step, ou
 
 
 def _verify(fn, cu_drafts, draft_logits, target_logits, draft_tokens, temperature, kmax, seed,
-            step, out=None, diag=False, stream=None, workspace=True):
+            step, out=None, diag=False, stream=None, workspace=True, t2d=None):
     """Marshals one verify call.  ``out`` (returned, and reusable by later calls of the same B
     and kmax on the same stream) holds the four result tensors and the device workspace; a
     workspace the caller puts in ``out["workspace"]`` must have been zero-filled before its
@@ -263,7 +269,13 @@ def _verify(fn, cu_drafts, draft_logits, target_logits, draft_tokens, temperatur
     _dev(temperature, "temperature", torch.float32)
     B = cu_drafts.numel() - 1
     V = target_logits.shape[1]
-    if draft_logits.dim() != 2 or (draft_logits.shape[0] > 0 and draft_logits.shape[1] != V):
+    if t2d is not None:
+        _dev(t2d, "t2d", torch.int32)
+        if t2d.numel() != V:
+            raise ValueError("t2d must be [V]")
+        if draft_logits.dim() != 2:
+            raise ValueError("draft_logits must be [rows, K]")
+    elif draft_logits.dim() != 2 or (draft_logits.shape[0] > 0 and draft_logits.shape[1] != V):
         raise ValueError("draft_logits must be [rows, V]")
     if temperature.numel() != B:
         raise ValueError("temperature must be [B]")
@@ -303,7 +315,10 @@ def _verify(fn, cu_drafts, draft_logits, target_logits, draft_tokens, temperatur
     a.diag = out["diag"].data_ptr() if out.get("diag") is not None else None
     a.workspace = ws.data_ptr() if ws is not None else None
     a.workspace_bytes = ws.numel() if ws is not None else 0
-    _check(fn(ctypes.byref(a), _stream(stream)))
+    if t2d is not None:
+        _check(fn(ctypes.byref(a), _ptr(t2d), int(draft_logits.shape[1]), _stream(stream)))
+    else:
+        _check(fn(ctypes.byref(a), _stream(stream)))
     return out
 
 
@@ -319,6 +334,22 @@ def spec_verify_block(cu_drafts, draft_logits, target_logits, draft_tokens, temp
     """Block verification (see include/specverify.h)."""
     return _verify(lib().spec_verify_block, cu_drafts, draft_logits, target_logits,
                    draft_tokens, temperature, kmax, seed, step, out, diag, stream)
+
+
+def spec_verify_tokenwise_reduced(cu_drafts, draft_logits, t2d, target_logits, draft_tokens, temperature,
+                                  kmax, seed, step, out=None, diag=False, stream=None):
+    """Token-wise verify with draft rows over a reduced draft vocabulary: draft_logits [rows, K],
+    t2d [V] int32 (the draft id of each target column, -1 outside the draft vocabulary)."""
+    return _verify(lib().spec_verify_tokenwise_reduced, cu_drafts, draft_logits, target_logits,
+                   draft_tokens, temperature, kmax, seed, step, out, diag, stream, t2d=t2d)
+
+
+def spec_verify_block_reduced(cu_drafts, draft_logits, t2d, target_logits, draft_tokens, temperature, kmax,
+                              seed, step, out=None, diag=False, stream=None):
+    """Block verification with draft rows over a reduced draft vocabulary (see
+    spec_verify_tokenwise_reduced)."""
+    return _verify(lib().spec_verify_block_reduced, cu_drafts, draft_logits, target_logits,
+                   draft_tokens, temperature, kmax, seed, step, out, diag, stream, t2d=t2d)
 
 
 def spec_verify_block_static(cu_drafts, draft_logits, target_logits, draft_tokens, temperature,

@@ -110,11 +110,25 @@ __device__ __forceinline__ double warp_incl_scan_d(double v, int lane) {
 template <typename T, int E>
 struct Chunk;
 
+// A chunk of a row may also be gathered: element e of chunk k is row[t2d[8 k + e]], or -inf
+// where t2d holds no index in [0, K) (a reduced draft vocabulary seen in target columns).
+__device__ __forceinline__ bool in_vocab(int j, int32_t K) { return (unsigned)j < (unsigned)K; }
+
 template <>
 struct Chunk<__nv_bfloat16, 8> {
     uint4 raw;
     __device__ __forceinline__ void load(const void* row, int64_t chunk) {
         raw = __ldg(reinterpret_cast<const uint4*>(row) + chunk);
+    }
+    __device__ __forceinline__ void gather(const void* row, const int32_t* t2d, int32_t K, int64_t chunk) {
+        const int4 a = __ldg(reinterpret_cast<const int4*>(t2d) + 2 * chunk);
+        const int4 b = __ldg(reinterpret_cast<const int4*>(t2d) + 2 * chunk + 1);
+        const int j[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const unsigned short* r = reinterpret_cast<const unsigned short*>(row);
+        uint32_t h[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h[e] = in_vocab(j[e], K) ? (uint32_t)__ldg(r + j[e]) : 0xff80u;   // bf16 -inf
+        raw = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
     }
     __device__ __forceinline__ void unpack(float (&x)[8]) const {
         x[0] = bf16_lo(raw.x); x[1] = bf16_hi(raw.x);
@@ -132,6 +146,16 @@ struct Chunk<float, 8> {
         a = __ldg(p);
         b = __ldg(p + 1);
     }
+    __device__ __forceinline__ void gather(const void* row, const int32_t* t2d, int32_t K, int64_t chunk) {
+        const int4 ja = __ldg(reinterpret_cast<const int4*>(t2d) + 2 * chunk);
+        const int4 jb = __ldg(reinterpret_cast<const int4*>(t2d) + 2 * chunk + 1);
+        const float* r = reinterpret_cast<const float*>(row);
+        const float ninf = __int_as_float(0xff800000);
+        a = make_float4(in_vocab(ja.x, K) ? __ldg(r + ja.x) : ninf, in_vocab(ja.y, K) ? __ldg(r + ja.y) : ninf,
+                        in_vocab(ja.z, K) ? __ldg(r + ja.z) : ninf, in_vocab(ja.w, K) ? __ldg(r + ja.w) : ninf);
+        b = make_float4(in_vocab(jb.x, K) ? __ldg(r + jb.x) : ninf, in_vocab(jb.y, K) ? __ldg(r + jb.y) : ninf,
+                        in_vocab(jb.z, K) ? __ldg(r + jb.z) : ninf, in_vocab(jb.w, K) ? __ldg(r + jb.w) : ninf);
+    }
     __device__ __forceinline__ void unpack(float (&x)[8]) const {
         x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
         x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
@@ -144,6 +168,10 @@ struct Chunk<__nv_bfloat16, 1> {
     __device__ __forceinline__ void load(const void* row, int64_t chunk) {
         raw = __ldg(reinterpret_cast<const unsigned short*>(row) + chunk);
     }
+    __device__ __forceinline__ void gather(const void* row, const int32_t* t2d, int32_t K, int64_t chunk) {
+        const int j = __ldg(t2d + chunk);
+        raw = in_vocab(j, K) ? __ldg(reinterpret_cast<const unsigned short*>(row) + j) : (uint16_t)0xff80u;
+    }
     __device__ __forceinline__ void unpack(float (&x)[1]) const {
         x[0] = __uint_as_float((uint32_t)raw << 16);
     }
@@ -154,6 +182,10 @@ struct Chunk<float, 1> {
     float v;
     __device__ __forceinline__ void load(const void* row, int64_t chunk) {
         v = __ldg(reinterpret_cast<const float*>(row) + chunk);
+    }
+    __device__ __forceinline__ void gather(const void* row, const int32_t* t2d, int32_t K, int64_t chunk) {
+        const int j = __ldg(t2d + chunk);
+        v = in_vocab(j, K) ? __ldg(reinterpret_cast<const float*>(row) + j) : __int_as_float(0xff800000);
     }
     __device__ __forceinline__ void unpack(float (&x)[1]) const { x[0] = v; }
 };

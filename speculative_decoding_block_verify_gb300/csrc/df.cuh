@@ -134,4 +134,20 @@ __device__ __forceinline__ df df_exp2(df x) {
     return df_scale(df_scale(p, pow2_int(n + 64.f)), 0x1p-64f);
 }
 
+// log2(e) / T as a df (T > 0) whose low part is strictly positive, so that x (hi + lo) with
+// x = -inf is -inf in both products: a low part of either sign, or zero, would give
+// -inf + inf = NaN for a -inf logit (a masked column, or one outside a reduced draft
+// vocabulary).  A non-positive low part takes one unit in the last place from the high part
+// (an exact move up to the low part's own rounding, ~2^-48 relative).
+__device__ __forceinline__ df temperature_scale(float T) {
+    const df l2e{1.4426950216293335f, 1.925963033500011e-08f};
+    df a = df_div(l2e, df_make(T));
+    if (!(a.lo > 0.f)) {
+        const float h = __int_as_float(__float_as_int(a.hi) - 1);   // hi > 0: the next float toward 0
+        a.lo = a.lo + (a.hi - h);
+        a.hi = h;
+    }
+    return a;
+}
+
 }  // namespace sv

@@ -32,6 +32,15 @@ __device__ __forceinline__ void resid_weights(const float (&xq)[E], const float 
     }
 }
 
+// Draft chunk k: read from the draft row, or - over a reduced draft vocabulary (t2d given) -
+// gathered through the column map.
+template <typename DQ, int E>
+__device__ __forceinline__ void load_q_chunk(Chunk<DQ, E>& c, const void* rq, int64_t k, const int32_t* t2d,
+                                             int32_t Kv) {
+    if (t2d) c.gather(rq, t2d, Kv, k);
+    else c.load(rq, k);
+}
+
 // Fixed-point weight (times `scale`) of each element of one chunk pair.
 template <typename DQ, typename DP, int E, bool BONUS>
 __device__ __forceinline__ void rescan_weights(const Chunk<DQ, E>& cq, const Chunk<DP, E>& cp, float Kq, float Kp,
@@ -59,7 +68,7 @@ __device__ __forceinline__ void rescan_weights(const Chunk<DQ, E>& cq, const Chu
 template <typename DQ, typename DP, int E, bool BONUS>
 __device__ __noinline__ int rescan_segment(const void* rq, const void* rp, int64_t c0, int64_t c1, float Kq,
                                            float Kp, float ah, float al, float c, float scale, unsigned long long t,
-                                           int lane) {
+                                           int lane, const int32_t* t2d, int32_t Kv) {
     // chunks per lane and group: bf16 rows 4, wider rows fewer (two groups stay in registers)
     constexpr int CB = E * (int)((BONUS ? 0 : sizeof(DQ)) + sizeof(DP));   // bytes per chunk (pair)
     constexpr int U = (E == 1) ? 4 : (CB <= 32 ? 2 : 1);
@@ -71,7 +80,7 @@ __device__ __noinline__ int rescan_segment(const void* rq, const void* rp, int64
         for (int u = 0; u < U; ++u) {
             const int64_t k = base + u * 32 + lane;
             if (k < c1) {
-                if (!BONUS) cq[u].load(rq, k);
+                if (!BONUS) load_q_chunk(cq[u], rq, k, t2d, Kv);
                 cp[u].load(rp, k);
             }
         }
@@ -163,7 +172,7 @@ __device__ __noinline__ int rescan_segment(const void* rq, const void* rp, int64
 template <typename DQ, typename DP, int E, bool BONUS>
 __device__ __noinline__ void segment_fixed_sum(const void* rq, const void* rp, int64_t k0, int64_t k1, float Kq,
                                                float Kp, float ah, float al, float c, float scale, int lane,
-                                               unsigned long long& sum, int& last) {
+                                               unsigned long long& sum, int& last, const int32_t* t2d, int32_t Kv) {
     constexpr int U = 2;
     unsigned long long ls = 0;
     int lp = -1;
@@ -174,7 +183,7 @@ __device__ __noinline__ void segment_fixed_sum(const void* rq, const void* rp, i
         for (int u = 0; u < U; ++u) {
             const int64_t k = base + u * 32 + lane;
             if (k < k1) {
-                if (!BONUS) cq[u].load(rq, k);
+                if (!BONUS) load_q_chunk(cq[u], rq, k, t2d, Kv);
                 cp[u].load(rp, k);
             }
         }

@@ -72,6 +72,11 @@ struct VerifyParams {
     char* list;          // the sweep's work list: the end of the workspace the caller passed
     int32_t dense;       // 1: logits and tokens in the dense [B, kmax (+1)] layout (see below)
     const uint64_t* step_dev;   // non-null: the Philox step is read from here (graph replays)
+    // draft rows over a reduced draft vocabulary: Kq logits per draft row, target column v
+    // holds draft id t2d[v] (none when t2d[v] lies outside [0, Kq)); t2d null: Kq = V
+    const int32_t* t2d;
+    int32_t Kq;
+    int64_t nchunk_q;    // chunks per draft row (= nchunk unless t2d is given)
 };
 
 // Logit rows of (stream b, slot i).  Packed layout (the public verify calls): draft row
@@ -85,6 +90,29 @@ __device__ __forceinline__ int64_t prow_of(const VerifyParams& p, int b, int bas
     return p.dense ? (int64_t)b * (p.kmax + 1) + i : (int64_t)base + b + i;
 }
 __device__ __forceinline__ uint64_t step_of(const VerifyParams& p) { return p.step_dev ? *p.step_dev : p.step; }
+
+// Draft logit of target column x in draft row `row` (-inf outside a reduced draft vocabulary).
+template <typename DQ>
+__device__ __forceinline__ float draft_logit_at(const VerifyParams& p, const void* row, int x) {
+    if (p.t2d == nullptr) return load_elem<DQ>(row, x);
+    const int j = __ldg(p.t2d + x);
+    return in_vocab(j, p.Kq) ? load_elem<DQ>(row, j) : -__int_as_float(0x7f800000);
+}
+
+// Geometry of the stats pass: the chunks of all stats rows, stream by stream (target rows of
+// nchunk chunks, then draft rows of nchunk_q), enumerated in one range.  Offset of stream b's
+// first row: cu[b] + b target rows and cu[b] draft rows lie before it.
+__device__ __forceinline__ int64_t stream_off(const VerifyParams& p, int b) {
+    return ((int64_t)p.cu[b] + b) * p.nchunk + (int64_t)p.cu[b] * p.nchunk_q;
+}
+// Offset and length of stats row j of stream b (j <= N: target row j, else draft row j - N - 1).
+__device__ __forceinline__ int64_t row_off(const VerifyParams& p, int b, int N, int j) {
+    const int64_t o = stream_off(p, b);
+    return j <= N ? o + (int64_t)j * p.nchunk : o + (int64_t)(N + 1) * p.nchunk + (int64_t)(j - N - 1) * p.nchunk_q;
+}
+__device__ __forceinline__ int64_t row_len(const VerifyParams& p, int N, int j) {
+    return j <= N ? p.nchunk : p.nchunk_q;
+}
 
 // Per-piece partial of one row.  T > 0: K = integer reference, (s_hi, s_lo) = sum 2^(l a - K).
 // T = 0: K = the piece maximum, idx = its lowest index.
@@ -587,10 +615,7 @@ __device__ __forceinline__ void stats_piece(StatsRing& ring, const void* row, in
 }
 
 // a = log2(e) / T as a df
-__device__ __forceinline__ df scale_of_temperature(float T) {
-    const df l2e{1.4426950216293335f, 1.925963033500011e-08f};
-    return df_div(l2e, df_make(T));
-}
+__device__ __forceinline__ df scale_of_temperature(float T) { return temperature_scale(T); }
 
 __device__ __forceinline__ bool temperature_ok(float T) { return isfinite(T) && (T == 0.f || T >= FLT_MIN); }
 
@@ -612,27 +637,36 @@ __device__ __forceinline__ int stream_of_row(const VerifyParams& p, int64_t rho,
 // batch-64 bf16 call (~50 KB per warp) any tail costs more than the end-time spread it removes,
 // on the batch-256 fp32 call (~690 KB per warp) a fifth of the rows as tail saves ~10%.  So the
 // tail is a fifth of the rows when a warp's share is at least kTailMinChunks chunks, else empty.
+// Draft rows over a reduced draft vocabulary are shorter than target rows; their calls take
+// every row static (the tail's fixed pieces assume one row length).
 constexpr int64_t kTailMinChunks = 16384;
-__host__ __device__ inline int64_t static_rows(int64_t rows, int64_t n, int64_t warps) {
+__host__ __device__ inline int64_t static_rows(int64_t rows, int64_t n, int64_t warps, bool reduced) {
+    if (reduced) return rows;
     return (rows * n >= kTailMinChunks * warps) ? rows * 4 / 5 : rows;
 }
 __host__ __device__ inline int64_t tail_pieces_per_row(int64_t n, int64_t seg_chunks) {
     const int64_t pc = 2 * seg_chunks;
     return (n + pc - 1) / pc;
 }
-// Chunks per warp of the static rows: equal shares, but at least ceil(n / (kPiecesMax - 2)) so
-// that no row is cut into more than kPiecesMax pieces.
-__host__ __device__ inline int64_t stats_share(int64_t rows, int64_t n, int64_t nw) {
-    const int64_t lw = (rows * n + nw - 1) / nw;
-    const int64_t lmin = (n + kPiecesMax - 3) / (kPiecesMax - 2);
+// Chunks per warp of the static range (`total` chunks): equal shares, but at least
+// ceil(nmax / (kPiecesMax - 2)) (nmax the longest row) so that no row is cut into more than
+// kPiecesMax pieces.
+__host__ __device__ inline int64_t stats_share(int64_t total, int64_t nmax, int64_t nw) {
+    const int64_t lw = (total + nw - 1) / nw;
+    const int64_t lmin = (nmax + kPiecesMax - 3) / (kPiecesMax - 2);
     return lw > lmin ? lw : (lmin > 0 ? lmin : 1);
 }
-// The pieces of stats row rho.  A static row (rho < rs): warps first .. first + count - 1,
-// warp gw's partial is piece gw - first; a tail row: tail_pieces_per_row fixed pieces.
-__device__ __forceinline__ int row_piece_count(int64_t rho, int64_t n, int64_t lw, int64_t rs, int64_t seg_chunks) {
-    if (rho >= rs) return (int)tail_pieces_per_row(n, seg_chunks);
-    const int64_t first = rho * n / lw;
-    return (int)((rho * n + n - 1) / lw - first) + 1;
+// The pieces of a stats row at offset `off` with `len` chunks.  A static row: warps
+// first .. first + count - 1, warp gw's partial is piece gw - first; a tail row:
+// tail_pieces_per_row fixed pieces.
+__device__ __forceinline__ int row_piece_count(bool tail, int64_t off, int64_t len, int64_t lw, int64_t seg_chunks) {
+    if (tail) return (int)tail_pieces_per_row(len, seg_chunks);
+    const int64_t first = off / lw;
+    return (int)((off + len - 1) / lw - first) + 1;
+}
+// The static range of a call: rs rows of nchunk chunks, or every row (reduced vocabulary).
+__device__ __forceinline__ int64_t static_total(const VerifyParams& p, int L, int64_t rs) {
+    return p.t2d ? stream_off(p, L) : rs * p.nchunk;
 }
 
 template <typename DQ, typename DP, int E>
@@ -654,9 +688,11 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) stats_kernel(c
     }
     if (L == 0) return;
     const int64_t n = p.nchunk;
+    const bool reduced = p.t2d != nullptr;
     const int64_t rows = 2 * (int64_t)p.cu[L] + L;
-    const int64_t rs = static_rows(rows, n, p.stats_warps);
-    const int64_t lw = stats_share(rs, n, p.stats_warps);
+    const int64_t rs = static_rows(rows, n, p.stats_warps, reduced);
+    const int64_t stot = static_total(p, L, rs);
+    const int64_t lw = stats_share(stot, max(n, p.nchunk_q), p.stats_warps);
     const int64_t gw = (int64_t)blockIdx.x * kStatsWarps + warp;
     const int64_t V = p.V;
     int b = 0;
@@ -688,7 +724,7 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) stats_kernel(c
         char* blk = row_block(p, rho);
         Part* dst = blk_at<Part>(blk, kOffParts) + slot;
         if (draft)
-            stats_piece<DQ, E>(ring, row_ptr<DQ>(p.dq, qrow_of(p, b, p.cu[b], (int)(j - Nb - 1)), V), c, c_end, false, ah, al,
+            stats_piece<DQ, E>(ring, row_ptr<DQ>(p.dq, qrow_of(p, b, p.cu[b], (int)(j - Nb - 1)), p.Kq), c, c_end, false, ah, al,
                                lane, dst, after_last);
         else
             stats_piece<DP, E>(ring, row_ptr<DP>(p.dp, prow_of(p, b, p.cu[b], (int)j), V), c, c_end, greedy, ah, al, lane,
@@ -698,8 +734,8 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) stats_kernel(c
     auto nothing = []() {};
     // ---- this warp's static share
     int64_t f = gw * lw;
-    const int64_t f1 = min(f + lw, rs * n);
-    if (f < f1) {
+    const int64_t f1 = min(f + lw, stot);
+    if (f < f1 && !reduced) {   // rows of one length: row f / n
         int64_t rho = f / n;
         int64_t c = f - rho * n;
         while (f < f1) {
@@ -708,6 +744,31 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) stats_kernel(c
             f += c_end - c;
             c = 0;
             ++rho;
+        }
+    } else if (f < f1) {        // target and draft rows of different lengths, stream by stream
+        int lo = 0, hi = L - 1;   // the stream holding chunk f: the last sb with stream_off(sb) <= f
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (stream_off(p, mid) <= f) lo = mid;
+            else hi = mid - 1;
+        }
+        int sb = lo;
+        int Ns = p.cu[sb + 1] - p.cu[sb];
+        const int64_t d = f - stream_off(p, sb), tp = (int64_t)(Ns + 1) * n;
+        int j = d < tp ? (int)(d / n) : Ns + 1 + (int)((d - tp) / p.nchunk_q);
+        int64_t roff = row_off(p, sb, Ns, j);
+        int64_t c = f - roff;
+        while (f < f1) {
+            const int64_t len = row_len(p, Ns, j);
+            const int64_t c_end = min(len, c + (f1 - f));
+            piece(2 * (int64_t)p.cu[sb] + sb + j, c, c_end, (int)(gw - roff / lw), nothing);
+            f += c_end - c;
+            c = 0;
+            roff += len;
+            if (++j > 2 * Ns) {   // the stream's last row: on to the next stream's first
+                j = 0;
+                if (++sb < L) Ns = p.cu[sb + 1] - p.cu[sb];
+            }
         }
     }
     // ---- the tail: fixed pieces claimed one by one from kTailTickets ranges (a warp starts on
@@ -811,7 +872,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const VerifyParams p) 
         sh.x[tid] = xi;
         bad_tok = (xi < 0 || xi >= p.V);
         if (!bad_tok && !greedy) {
-            sh.lq[tid] = load_elem<DQ>(row_ptr<DQ>(p.dq, qrow_of(p, b, base, tid), V), xi);
+            sh.lq[tid] = draft_logit_at<DQ>(p, row_ptr<DQ>(p.dq, qrow_of(p, b, base, tid), p.Kq), xi);
             sh.lp[tid] = load_elem<DP>(row_ptr<DP>(p.dp, prow_of(p, b, base, tid), V), xi);
         }
     }
@@ -821,8 +882,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const VerifyParams p) 
     WsHeader* hdr = ws_header(p);
     if (!offsets_ok) return;   // finish_kernel reports BAD_OFFSETS
     const int L = __ldcg(&hdr->L);
-    const int64_t rs = static_rows(2 * (int64_t)p.cu[L] + L, p.nchunk, p.stats_warps);
-    const int64_t lw = stats_share(rs, p.nchunk, p.stats_warps);
+    const int64_t rs = static_rows(2 * (int64_t)p.cu[L] + L, p.nchunk, p.stats_warps, p.t2d != nullptr);
+    const int64_t lw = stats_share(static_total(p, L, rs), max(p.nchunk, p.nchunk_q), p.stats_warps);
     const int64_t gb = 2 * (int64_t)base + b;
     const int nrows = 2 * N + 1;
     const bool reduce_rows = temp_ok && !bad_tok;
@@ -834,7 +895,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const VerifyParams p) 
         for (int r = (greedy ? N : 0) + warp; r < nrows; r += kWarps) {
             const int64_t rho = stats_row_of_part(gb, N, r);
             char* blk = row_block(p, rho);
-            const int cnt_want = row_piece_count(rho, p.nchunk, lw, rs, p.seg_chunks);
+            const int cnt_want = row_piece_count(rho >= rs, row_off(p, b, N, (int)(rho - gb)), row_len(p, N, (int)(rho - gb)),
+                                                 lw, p.seg_chunks);
             const unsigned cnt = __ldcg(blk_at<unsigned>(blk, kOffStatsCount));
             Part e[2];
 #pragma unroll
@@ -1163,7 +1225,8 @@ __device__ __forceinline__ void sweep_segments(SweepRing<DQ, DP, E>& R, const Ve
         const int64_t left = seg_end - c0;
         n = left <= 0 ? 0 : (int)(left < G ? left : G);
     };
-    const void* q = bonus ? nullptr : rq;
+    const bool gather_q = !bonus && p.t2d != nullptr;   // reduced draft vocabulary: q is gathered
+    const void* q = (bonus || gather_q) ? nullptr : rq;
     auto issue = [&](int t) {
         if (t < nst) {
             int64_t c0;
@@ -1174,18 +1237,47 @@ __device__ __forceinline__ void sweep_segments(SweepRing<DQ, DP, E>& R, const Ve
         }
     };
     for (int t = 0; t < D - 1; ++t) issue(t);
+    // reduced draft vocabulary: the draft chunks of a stage are gathered through the column
+    // map, all of a lane's at once, one stage ahead (in flight while the stage before is summed)
+    constexpr int UQ = (G + 31) / 32;
+    Chunk<DQ, E> cq_cur[UQ], cq_nxt[UQ];
+    auto gather_stage = [&](int t, Chunk<DQ, E>(&cq)[UQ]) {
+        int64_t c0;
+        int n;
+        stage(t, c0, n);
+#pragma unroll
+        for (int u = 0; u < UQ; ++u)
+            if (lane + 32 * u < n) cq[u].gather(rq, p.t2d, p.Kq, c0 + lane + 32 * u);
+    };
+    if (gather_q && nst > 0) gather_stage(0, cq_cur);
     Kahan acc;
     for (int t = 0; t < nst; ++t) {
         issue(t + D - 1);
         int64_t c0;
         int n;
         stage(t, c0, n);
+        if (gather_q && t + 1 < nst) gather_stage(t + 1, cq_nxt);
         R.wait(t % D, n);
         float grp = 0.f;   // this lane's chunk sums of the stage (independent), added once
-        for (int kk = lane; kk < n; kk += 32) {
-            float xq[E], xp[E];
-            R.get(t % D, kk, rq, rp, c0, !bonus, xq, xp);
-            grp += bonus ? target_chunk_sum<E>(xp, Kp, ah, al) : resid_chunk_sum<E>(xq, xp, Kq, Kp, ah, al, cc);
+        if (gather_q) {
+#pragma unroll
+            for (int u = 0; u < UQ; ++u) {
+                const int kk = lane + 32 * u;
+                if (kk < n) {
+                    float xq[E], xp[E];
+                    R.get(t % D, kk, rq, rp, c0, false, xq, xp);
+                    cq_cur[u].unpack(xq);
+                    grp += resid_chunk_sum<E>(xq, xp, Kq, Kp, ah, al, cc);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UQ; ++u) cq_cur[u] = cq_nxt[u];
+        } else {
+            for (int kk = lane; kk < n; kk += 32) {
+                float xq[E], xp[E];
+                R.get(t % D, kk, rq, rp, c0, !bonus, xq, xp);
+                grp += bonus ? target_chunk_sum<E>(xp, Kp, ah, al) : resid_chunk_sum<E>(xq, xp, Kq, Kp, ah, al, cc);
+            }
         }
         acc.add(grp);
         if (t % mps == mps - 1) {   // the segment is complete
@@ -1240,7 +1332,7 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const VerifyParams p
         unsigned long long nxt = total;
         int nword = 0;
         const int64_t gb = 2 * (int64_t)p.cu[b] + b;
-        const void* rq = bonus ? nullptr : row_ptr<DQ>(p.dq, qrow_of(p, b, p.cu[b], i), V);
+        const void* rq = bonus ? nullptr : row_ptr<DQ>(p.dq, qrow_of(p, b, p.cu[b], i), p.Kq);
         const void* rp = row_ptr<DP>(p.dp, prow_of(p, b, p.cu[b], i), V);
         const int s1 = min(p.nseg, s0 + kSegsPerClaim);
         // once this claim's last copy is issued: the next claim's entry is loaded while the
@@ -1387,7 +1479,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) 
     const float ah = sh.a_hi, al = sh.a_lo;
     const df one{1.f, 0.f};
     const bool block = (p.rule == 1);
-    auto qrow = [&](int i) { return row_ptr<DQ>(p.dq, qrow_of(p, b, base, i), V); };
+    auto qrow = [&](int i) { return row_ptr<DQ>(p.dq, qrow_of(p, b, base, i), p.Kq); };
     auto prow = [&](int i) { return row_ptr<DP>(p.dp, prow_of(p, b, base, i), V); };
 
     if (sh.status == SPEC_ST_OK && !greedy && sh.n_pass > 0) {
@@ -1494,10 +1586,10 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) 
             int last;
             if (bonus)
                 segment_fixed_sum<DQ, DP, E, true>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, lane, sub,
-                                                   last);
+                                                   last, p.t2d, p.Kq);
             else
                 segment_fixed_sum<DQ, DP, E, false>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, lane, sub,
-                                                    last);
+                                                    last, p.t2d, p.Kq);
             if (lane == 0) {
                 sh.sub_sum[warp] = sub;
                 sh.sub_last[warp] = last;
@@ -1518,9 +1610,9 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) 
                 y = lastpos;   // rounding kept the segment's sum at or below the target
             } else if (warp == wsel) {
                 y = bonus ? rescan_segment<DQ, DP, E, true>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale,
-                                                            t - before, lane)
+                                                            t - before, lane, p.t2d, p.Kq)
                           : rescan_segment<DQ, DP, E, false>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale,
-                                                             t - before, lane);
+                                                             t - before, lane, p.t2d, p.Kq);
             }
             if ((wsel < 0 && tid == 0) || (warp == wsel && lane == 0)) p.out_tok[ob + tau] = y;
         }
@@ -1713,9 +1805,13 @@ static int check_args(const spec_verify_args* a, const char* name, bool need_poi
     return SPEC_OK;
 }
 
-static int verify_entry(const spec_verify_args* a, void* stream, int rule, const char* name, int* info) {
+static int verify_entry(const spec_verify_args* a, void* stream, int rule, const char* name, int* info,
+                        const int32_t* t2d = nullptr, int32_t Kq = 0) {
     int rc = check_args(a, name, info == nullptr);
     if (rc != SPEC_OK) return rc;
+    const bool reduced = t2d != nullptr;
+    if (reduced && (Kq < 1 || Kq > a->V))
+        return set_error(SPEC_ERR_SHAPE, "%s: draft vocabulary K = %d outside [1, V = %d]", name, Kq, a->V);
     if (info == nullptr && a->B == 0) return clear_error();
     VerifyParams p;
     p.B = a->B;
@@ -1736,9 +1832,13 @@ static int verify_entry(const spec_verify_args* a, void* stream, int rule, const
     p.diag = a->diag;
     p.dense = 0;
     p.step_dev = nullptr;
+    p.t2d = t2d;
+    p.Kq = reduced ? Kq : a->V;
     const bool aligned = (a->V % 8 == 0) && ((uintptr_t)a->target_logits % 16 == 0) &&
-                         ((uintptr_t)a->draft_logits % 16 == 0);
+                         ((uintptr_t)a->draft_logits % 16 == 0) &&
+                         (!reduced || (Kq % 8 == 0 && (uintptr_t)t2d % 16 == 0));
     p.nchunk = aligned ? a->V / 8 : a->V;
+    p.nchunk_q = aligned ? p.Kq / 8 : p.Kq;
     p.seg_chunks = (p.nchunk + kSegs - 1) / kSegs;
     p.nseg = (int32_t)((p.nchunk + p.seg_chunks - 1) / p.seg_chunks);
     p.ws = reinterpret_cast<char*>(a->workspace);
@@ -1785,9 +1885,12 @@ int verify_dense_launch(int rule, const spec_verify_args* a, const uint64_t* ste
     p.diag = a->diag;
     p.dense = 1;
     p.step_dev = step_dev;
+    p.t2d = nullptr;
+    p.Kq = a->V;
     const bool aligned = (a->V % 8 == 0) && ((uintptr_t)a->target_logits % 16 == 0) &&
                          ((uintptr_t)a->draft_logits % 16 == 0);
     p.nchunk = aligned ? a->V / 8 : a->V;
+    p.nchunk_q = p.nchunk;
     p.seg_chunks = (p.nchunk + kSegs - 1) / kSegs;
     p.nseg = (int32_t)((p.nchunk + p.seg_chunks - 1) / p.seg_chunks);
     p.ws = reinterpret_cast<char*>(a->workspace);
@@ -1814,6 +1917,18 @@ extern "C" int spec_verify_tokenwise(const spec_verify_args* args, void* stream)
 
 extern "C" int spec_verify_block(const spec_verify_args* args, void* stream) {
     return sv::verify_entry(args, stream, 1, "spec_verify_block", nullptr);
+}
+
+extern "C" int spec_verify_tokenwise_reduced(const spec_verify_args* args, const int32_t* t2d, int32_t K,
+                                             void* stream) {
+    if (t2d == nullptr) return sv::set_error(SPEC_ERR_ARG, "spec_verify_tokenwise_reduced: t2d is NULL");
+    return sv::verify_entry(args, stream, 0, "spec_verify_tokenwise_reduced", nullptr, t2d, K);
+}
+
+extern "C" int spec_verify_block_reduced(const spec_verify_args* args, const int32_t* t2d, int32_t K,
+                                         void* stream) {
+    if (t2d == nullptr) return sv::set_error(SPEC_ERR_ARG, "spec_verify_block_reduced: t2d is NULL");
+    return sv::verify_entry(args, stream, 1, "spec_verify_block_reduced", nullptr, t2d, K);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -138,8 +138,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                 else if (an < 0 || an >= p.V) st = SPEC_ST_BAD_TOKEN;
                 greedy = (T == 0.f);
                 if (st == SPEC_ST_OK && !greedy) {
-                    const df l2e{1.4426950216293335f, 1.925963033500011e-08f};
-                    const df a = df_div(l2e, df_make(T));
+                    const df a = temperature_scale(T);
                     ah = a.hi;
                     al = a.lo;
                 }
@@ -399,7 +398,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                     unsigned long long sub;
                     int last;
                     segment_fixed_sum<float, f32_coherent, E, true>(nullptr, row, w0, w1, 0.f, s_K, s_ah[g], s_al[g],
-                                                                    0.f, s_scale, lane, sub, last);
+                                                                    0.f, s_scale, lane, sub, last, nullptr, 0);
                     if (lane == 0) {
                         s_sub[warp] = sub;
                         s_sub_last[warp] = last;
@@ -419,7 +418,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                     if (wsel < 0) y = lastpos;   // rounding kept the slice's sum at or below the target
                     else if (warp == wsel)
                         y = rescan_segment<float, f32_coherent, E, true>(nullptr, row, w0, w1, 0.f, s_K, s_ah[g],
-                                                                         s_al[g], 0.f, s_scale, tt - bef, lane);
+                                                                         s_al[g], 0.f, s_scale, tt - bef, lane, nullptr, 0);
                     if ((wsel < 0 && tid == 0) || (warp == wsel && lane == 0)) p.tokens[(int64_t)b * p.N + i] = y;
                 }
                 __syncthreads();

@@ -124,9 +124,12 @@ def _widen(rows, kind):
 
 
 def _stream_task(args):
-    runs, q_rows, kq, p_rows, kp, x, T, b = args
+    runs, q_rows, kq, p_rows, kp, x, T, b, t2d = args
     from oracle import verify as ov
     q = _widen(q_rows, kq)
+    if t2d is not None:   # draft rows over a reduced draft vocabulary, scattered into target columns
+        sc = ov.ScatteredRows(q, t2d)
+        q = [sc[i] for i in range(len(q))]
     p = _widen(p_rows, kp)
     return [ov.verify_stream(rule, q, p, x, T, seed, step, b) for rule, seed, step in runs]
 
@@ -150,13 +153,15 @@ def _host(a):
 
 def oracle_runs(d, kmax, runs, streams, torch, workers=None, runs_per_task=None):
     """Run the oracle for every (rule, seed, step) in ``runs`` over ``streams`` of the inputs
-    d = {cu, dq, dp, x, T} (device tensors; dq / dp may also be host arrays); returns
+    d = {cu, dq, dp, x, T} (device tensors; dq / dp may also be host arrays; an optional
+    ``t2d`` marks dq as rows over a reduced draft vocabulary); returns
     {(rule, seed, step): batch result like oracle.verify.verify_batch (only ``streams``
     filled)}.  A stream's runs are split into tasks of ``runs_per_task``."""
     from oracle import verify as ov
     cu = _host(d["cu"])
     x = _host(d["x"])
     T = _host(d["T"])
+    t2d = _host(d["t2d"]) if d.get("t2d") is not None else None
     B = len(cu) - 1
     first_bad = B
     for b in range(B):
@@ -173,7 +178,7 @@ def oracle_runs(d, kmax, runs, streams, torch, workers=None, runs_per_task=None)
         q, kq = device_rows(d["dq"], int(cu[b]), int(cu[b]) + n, torch)
         p, kp = device_rows(d["dp"], int(cu[b]) + b, int(cu[b]) + b + n + 1, torch)
         for k0 in range(0, len(runs), per):
-            tasks.append((runs[k0:k0 + per], q, kq, p, kp, x[cu[b]:cu[b] + n], float(T[b]), b))
+            tasks.append((runs[k0:k0 + per], q, kq, p, kp, x[cu[b]:cu[b] + n], float(T[b]), b, t2d))
             where.append((b, k0))
     workers = workers or max(1, min(len(tasks), len(os.sched_getaffinity(0))))
     with mp.get_context("spawn").Pool(workers) as pool:
