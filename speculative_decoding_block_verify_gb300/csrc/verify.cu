@@ -489,19 +489,20 @@ struct StatsRing {
             bulk_g2s_hint(base + slot * kStageBytes, src, bytes, &bar[slot], policy);
         }
     }
-    // Waits for the oldest copy in flight and returns its stage.
+    // Waits for the oldest copy in flight and returns its stage.  The outcome is decided for the
+    // whole warp (every lane takes the same path afterwards).
     __device__ __forceinline__ const char* wait() {
         const uint32_t slot = done % kStages;
         if (!timeout) {
             const uint32_t parity = (done / kStages) & 1u;
-            int n = 0;
-            while (!mbar_try_wait(&bar[slot], parity)) {
+            bool ok = true;
+            for (int n = 0; !mbar_try_wait(&bar[slot], parity);)
                 if (++n > kSpinLimit) {
-                    timeout = true;   // this copy stays outstanding; drain() waits for it once more
-                    return base + slot * kStageBytes;
+                    ok = false;
+                    break;
                 }
-            }
-            ++done;
+            timeout = !__all_sync(0xffffffffu, ok);   // a copy that timed out stays outstanding: drain() waits once more
+            if (!timeout) ++done;
         }
         return base + slot * kStageBytes;
     }
@@ -1148,13 +1149,14 @@ struct SweepRing<DQ, DP, 8> {
     __device__ __forceinline__ void wait(int slot, int n) {
         if (timeout || n <= 0) return;
         const unsigned parity = (phase >> slot) & 1u;
-        int k = 0;
-        while (!mbar_try_wait(&bar[slot], parity)) {
+        bool ok = true;
+        for (int k = 0; !mbar_try_wait(&bar[slot], parity);)
             if (++k > kSpinLimit) {
-                timeout = true;   // the slot stays pending; drain() waits for it once more
-                return;
+                ok = false;
+                break;
             }
-        }
+        timeout = !__all_sync(0xffffffffu, ok);   // one decision for the whole warp
+        if (timeout) return;                       // the slot stays pending; drain() waits for it once more
         phase ^= 1u << slot;
         pending &= ~(1u << slot);
     }

@@ -38,7 +38,9 @@ def bias_bound(d, w1, w2, prev):
 
 
 @pytest.mark.parametrize("case", [("tiny", None, None, None), ("single_bias", None, None, None),
-                                  ("tiny", 20, 1001, 24), ("single_bias", 9, 4096, 256)])
+                                  ("tiny", 20, 1001, 24), ("single_bias", 9, 4096, 256),
+                                  ("single_bias", 13, 4104, 100), ("tiny", 7, 2056, 3),
+                                  ("single_bias", 2, 8200, 40), ("single_bias", 3, 8192, 64)])
 def test_markov_bias_parity(case):
     name, rows, V, R = case
     inp = workloads.make_verify_inputs(name, 101, V=V)
