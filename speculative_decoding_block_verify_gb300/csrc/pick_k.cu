@@ -7,11 +7,15 @@
 // (al-engr.com), "The controller, and the table it reads from" (best expected tokens per
 // millisecond, cost from verify_ms[num_tokens]).
 //
-// Kernel 1: one CTA per stream, one warp per draft slot: the dot h . w streams the hidden
-// state once (16-byte loads, float32 accumulation), then sigmoid, cumulative product and -
-// in per-stream mode - the stream's own pick, all in float64 scalars.
-// Kernel 2: one CTA: batch mode's ordering of all (stream, slot) entries and its pick, then
-// the exclusive prefix sum that gives cu_drafts.
+// Kernel 1: one CTA (16 warps) per stream, `split` warps per draft slot (up to 4, as many as
+// 16 warps allow; with more than 16 slots a warp takes two): each warp takes a contiguous
+// share of the dot h . w with all of a lane's 16-byte loads in flight at once (float32
+// accumulation; at H = 7168 a lane's share is 7 chunks, so the hidden state streams in one
+// round trip), the shares are added in a fixed order, then one warp takes sigmoid, cumulative
+// product and - in per-stream mode - the stream's own pick, with scans across its lanes.
+// Kernel 2: one CTA, launched as a programmatic dependent of kernel 1 (its launch overlaps
+// kernel 1): batch mode's ordering of all (stream, slot) entries and its pick, then the
+// exclusive prefix sum that gives cu_drafts.
 
 #include <cfloat>
 #include <climits>
@@ -23,6 +27,8 @@ namespace sv {
 
 constexpr int kPickThreads = 1024;
 constexpr int kMaxBatchEntries = 4096;
+constexpr int kConfMaxSplit = 4;   // warps per dot product
+constexpr int kConfWarps = 16;     // warps of a confidence CTA: items (slot, share) go round them
 
 struct PickParams {
     const void* hidden;
@@ -35,23 +41,28 @@ struct PickParams {
     int32_t* k_out;
     int32_t* cu_out;
     int64_t nchunk;
+    int32_t split;   // warps per dot product
 };
 
 template <typename T, int E>
-__global__ void confidence_kernel(const PickParams p) {
-    __shared__ double c_s[SPEC_MAX_KMAX];
+__global__ void __launch_bounds__(kConfWarps * 32) confidence_kernel(const PickParams p) {
+    __shared__ float part_s[SPEC_MAX_KMAX * kConfMaxSplit];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int U = 4;
-    if (warp < p.kmax) {
-        const void* hrow = row_ptr<T>(p.hidden, (int64_t)b * p.kmax + warp, p.H);
+    const int64_t per = (p.nchunk + p.split - 1) / p.split;
+    constexpr int U = 16 / (int)sizeof(T);   // chunks per lane in flight at once (64 registers of h and w)
+    for (int item = warp; item < p.kmax * p.split; item += kConfWarps) {
+        const int slot = item / p.split, part = item - slot * p.split;
+        const int64_t k0 = min(p.nchunk, (int64_t)part * per), k1 = min(p.nchunk, k0 + per);
+        const void* hrow = row_ptr<T>(p.hidden, (int64_t)b * p.kmax + slot, p.H);
         float acc = 0.f;
-        for (int64_t base = 0; base < p.nchunk; base += 32 * U) {
+        for (int64_t base = k0; base < k1; base += 32 * U) {
             Chunk<T, E> ch[U], cw[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t k = base + u * 32 + lane;
-                if (k < p.nchunk) {
+                if (k < k1) {
                     ch[u].load(hrow, k);
                     cw[u].load(p.w, k);
                 }
@@ -59,7 +70,7 @@ __global__ void confidence_kernel(const PickParams p) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t k = base + u * 32 + lane;
-                if (k < p.nchunk) {
+                if (k < k1) {
                     float xh[E], xw[E];
                     ch[u].unpack(xh);
                     cw[u].unpack(xw);
@@ -69,28 +80,57 @@ __global__ void confidence_kernel(const PickParams p) {
             }
         }
         acc = warp_sum(acc);
-        if (lane == 0) {
-            const double x = (double)acc + p.bias;
-            c_s[warp] = (x >= 0.0) ? 1.0 / (1.0 + exp(-x)) : exp(x) / (1.0 + exp(x));
-        }
+        if (lane == 0) part_s[item] = acc;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        double a = 1.0, e_n = 1.0;
-        int best_n = 0;
-        double best = 1.0 / (double)p.verify_ms[1];
-        for (int j = 0; j < p.kmax; ++j) {
-            a *= c_s[j];
-            p.c_out[(int64_t)b * p.kmax + j] = (float)c_s[j];
-            p.a_out[(int64_t)b * p.kmax + j] = (float)a;
-            e_n += a;                                   // E_{j+1}
-            const double ratio = e_n / (double)p.verify_ms[j + 2];
-            if (ratio > best) {
-                best = ratio;
-                best_n = j + 1;
+    // the stream's tail in one warp (float32, exact-rounding exp and divide): lane j holds slot
+    // j: c_j, the prefix product a_j, E_{j+1} = 1 + a_0 + ... + a_j (scans across the lanes),
+    // and the controller's best n by E_n / verify_ms[n + 1] (ties -> the smaller n)
+    if (warp == 0) {
+        const int j = lane;
+        float cj = 1.f;
+        if (j < p.kmax) {
+            float dot = 0.f;
+            for (int q = 0; q < p.split; ++q) dot += part_s[j * p.split + q];   // a fixed order
+            const float x = dot + (float)p.bias;
+            cj = (x >= 0.f) ? 1.f / (1.f + expf(-x)) : expf(x) / (1.f + expf(x));
+        }
+        float a = cj;   // inclusive prefix product
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, a, o);
+            if (lane >= o) a *= n;
+        }
+        float sa = (j < p.kmax) ? a : 0.f;   // inclusive prefix sum of a
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, sa, o);
+            if (lane >= o) sa += n;
+        }
+        if (j < p.kmax) {
+            p.c_out[(int64_t)b * p.kmax + j] = cj;
+            p.a_out[(int64_t)b * p.kmax + j] = a;
+        }
+        // candidate n = j + 1 (lane j), n = 0 (lane 0 also holds it)
+        float best = (j < p.kmax) ? (1.f + sa) / p.verify_ms[j + 2] : -1.f;
+        int best_n = j + 1;
+        if (lane == 0) {
+            const float r0 = 1.f / p.verify_ms[1];
+            if (!(best > r0)) {
+                best = r0;
+                best_n = 0;
             }
         }
-        if (p.mode == 0) p.k_out[b] = best_n;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int on = __shfl_xor_sync(0xffffffffu, best_n, o);
+            if (ob > best || (ob == best && on < best_n)) {
+                best = ob;
+                best_n = on;
+            }
+        }
+        if (p.mode == 0 && lane == 0) p.k_out[b] = best_n;
     }
 }
 
@@ -123,6 +163,7 @@ __device__ void write_cu(const int32_t* k, int32_t* cu, int B) {
 }
 
 __global__ void __launch_bounds__(kPickThreads) pick_batch_kernel(const PickParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // every confidence CTA has finished
     __shared__ float a_s[kMaxBatchEntries];
     __shared__ uint16_t order[kMaxBatchEntries];   // order[rank] = entry
     __shared__ int k_s[kMaxBatchEntries];
@@ -205,12 +246,22 @@ __global__ void __launch_bounds__(kPickThreads) pick_batch_kernel(const PickPara
 }
 
 template <typename T, int E>
-static cudaError_t launch_pick(const PickParams& p, cudaStream_t s) {
-    confidence_kernel<T, E><<<p.B, 32 * p.kmax, 0, s>>>(p);
+static cudaError_t launch_pick(PickParams p, cudaStream_t s) {
+    p.split = kConfWarps / p.kmax < kConfMaxSplit ? kConfWarps / p.kmax : kConfMaxSplit;
+    if (p.split < 1) p.split = 1;
+    confidence_kernel<T, E><<<p.B, kConfWarps * 32, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    pick_batch_kernel<<<1, kPickThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kPickThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pick_batch_kernel, p);
 }
 
 }  // namespace sv

@@ -9,6 +9,7 @@ calls; nothing is timed or checked here - bench.py and the tests do that):
                            (stats_kernel, decide_kernel, sweep_kernel, finish_kernel)
   verify_tokenwise_batch64 spec_verify_tokenwise, the same inputs
   verify_block_batch256_k9 spec_verify_block, B = 256, k = 9, V = 129,280, fp32
+  verify_reduced_batch64_topk  spec_verify_block_reduced, B = 64, k = 5, V = 129,280, K = 32,768
   bias_single              dspark_markov_bias, 5 rows, rank 256, V = 129,280, bf16, with a
                            256 MB scrub before every call so that W2 is read from HBM
   walk_single              dspark_markov_walk, one stream, N = 5, rank 256, V = 129,280, bf16
@@ -44,7 +45,13 @@ def main(argv=None):
     torch.cuda.set_device(dev)
     sv.lib()
     total = a.warmup + a.calls
-    if a.case.startswith("verify_"):
+    if a.case == "verify_reduced_batch64_topk":
+        s = workloads.make_verify_inputs("batch64_topk", 3000, backend="torch", device=dev)
+        out = None
+        for i in range(total):
+            out = sv.spec_verify_block_reduced(s["cu_drafts"], s["draft_logits"], s["t2d"], s["target_logits"],
+                                               s["draft_tokens"], s["temperature"], s["kmax"], 0, i, out=out)
+    elif a.case.startswith("verify_"):
         rule, name = a.case.split("_", 2)[1:]
         fn = sv.spec_verify_block if rule == "block" else sv.spec_verify_tokenwise
         s = workloads.make_verify_inputs(name, 3000, backend="torch", device=dev)
