@@ -860,10 +860,12 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const VerifyParams p) 
         sh.u_acc[tid] = uniform24_df(wds.x);
     }
     if (tid <= SPEC_MAX_KMAX) sh.w[tid] = df{__int_as_float(0x7fffffff), 0.f};
-    // stream b has valid offsets iff no stream j <= b breaks the packed layout
-    bool broken = false;
-    for (int j = tid; j <= b; j += kThreads) broken |= offsets_bad(p, j);
-    const bool offsets_ok = !__syncthreads_or(broken);
+    // the valid stream prefix [0, L) (the stats grid computes the same from the same inputs) and,
+    // from it, the stats partition: all before the wait, while the stats grid streams
+    const int L = valid_prefix(p);
+    const bool offsets_ok = b < L;   // no stream j <= b breaks the packed layout
+    const int64_t rs = static_rows(2 * (int64_t)p.cu[L] + L, p.nchunk, p.stats_warps, p.t2d != nullptr);
+    const int64_t lw = stats_share(static_total(p, L, rs), max(p.nchunk, p.nchunk_q), p.stats_warps);
     const int base = p.cu[b];
     const int N = offsets_ok ? p.cu[b + 1] - base : 0;
     const int64_t V = p.V;
@@ -882,9 +884,6 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const VerifyParams p) 
 
     WsHeader* hdr = ws_header(p);
     if (!offsets_ok) return;   // finish_kernel reports BAD_OFFSETS
-    const int L = __ldcg(&hdr->L);
-    const int64_t rs = static_rows(2 * (int64_t)p.cu[L] + L, p.nchunk, p.stats_warps, p.t2d != nullptr);
-    const int64_t lw = stats_share(static_total(p, L, rs), max(p.nchunk, p.nchunk_q), p.stats_warps);
     const int64_t gb = 2 * (int64_t)base + b;
     const int nrows = 2 * N + 1;
     const bool reduce_rows = temp_ok && !bad_tok;
@@ -1402,6 +1401,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) 
     }
     const int base = p.cu[b];
     const int n_raw = p.cu[b + 1] - base;
+    const int L = valid_prefix(p);   // as the stats grid computed it, from the same inputs
     asm volatile("griddepcontrol.wait;" ::: "memory");
     WsHeader* hdr = ws_header(p);
     if (b == 0 && tid == 0) {   // every earlier grid of the call has finished: tickets back to zero
@@ -1409,7 +1409,6 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) 
         hdr->ticket_sweep = 0ull;
         hdr->sweep_total = 0ull;
     }
-    const int L = __ldcg(&hdr->L);
     if (b >= L) {
         for (int j = tid; j <= p.kmax; j += kThreads) p.out_tok[ob + j] = -1;
         if (tid == 0) {
