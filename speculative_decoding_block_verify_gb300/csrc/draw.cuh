@@ -167,6 +167,94 @@ __device__ __noinline__ int rescan_segment(const void* rq, const void* rp, int64
     return y >= 0 ? y : ylast;
 }
 
+// One warp's slice [k0, k1) (at most 64 chunks: two per lane) of the drawn segment, its
+// fixed-point weights loaded once: sum() gives the slice's total and last positive element
+// (every lane), rescan(t) - in the warp whose slice crosses the target - the first element
+// whose running sum exceeds t, from the same registers.  Chunk order and arithmetic are those
+// of segment_fixed_sum and rescan_segment (chunk k0 + 32 u + lane), so the token is the same.
+template <typename DQ, typename DP, int E, bool BONUS>
+struct DrawSlice {
+    unsigned long long qv[2][E];
+    unsigned long long lsum[2];
+    int lpos[2];
+    int64_t k0;
+    __device__ __forceinline__ void load(const void* rq, const void* rp, int64_t a, int64_t b, float Kq, float Kp,
+                                         float ah, float al, float c, float scale, int lane, const int32_t* t2d,
+                                         int32_t Kv) {
+        k0 = a;
+        Chunk<DQ, E> cq[2];
+        Chunk<DP, E> cp[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t k = a + u * 32 + lane;
+            if (k < b) {
+                if (!BONUS) load_q_chunk(cq[u], rq, k, t2d, Kv);
+                cp[u].load(rp, k);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t k = a + u * 32 + lane;
+            lsum[u] = 0;
+            lpos[u] = -1;
+#pragma unroll
+            for (int j = 0; j < E; ++j) qv[u][j] = 0;
+            if (k < b) {
+                rescan_weights<DQ, DP, E, BONUS>(cq[u], cp[u], Kq, Kp, ah, al, c, scale, qv[u]);
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    lsum[u] += qv[u][j];
+                    if (qv[u][j] > 0) lpos[u] = (int)(k * E + j);
+                }
+            }
+        }
+    }
+    __device__ __forceinline__ void sum(unsigned long long& total, int& last) const {
+        unsigned long long ls = lsum[0] + lsum[1];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+        total = ls;
+        last = __reduce_max_sync(0xffffffffu, max(lpos[0], lpos[1]));
+    }
+    __device__ __forceinline__ int rescan(unsigned long long t, int lane) const {
+        unsigned long long incl[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) incl[u] = lsum[u];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const unsigned long long n = __shfl_up_sync(0xffffffffu, incl[u], o);
+                if (lane >= o) incl[u] += n;
+            }
+        unsigned long long run = 0;
+        int ylast = -1;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const unsigned long long total = __shfl_sync(0xffffffffu, incl[u], 31);
+            const unsigned hit = __ballot_sync(0xffffffffu, lsum[u] > 0 && run + incl[u] > t);
+            const int lp_max = __reduce_max_sync(0xffffffffu, lpos[u]);
+            if (lp_max >= 0) ylast = lp_max;
+            if (hit) {
+                const int L = __ffs(hit) - 1;
+                int yl = -1;
+                if (lane == L) {
+                    unsigned long long acc = run + incl[u] - lsum[u];
+#pragma unroll
+                    for (int j = 0; j < E; ++j) {
+                        acc += qv[u][j];
+                        if (yl < 0 && qv[u][j] > 0 && acc > t) yl = (int)((k0 + u * 32 + lane) * E + j);
+                    }
+                    if (yl < 0) yl = lpos[u];
+                }
+                return __shfl_sync(0xffffffffu, yl, L);
+            }
+            run += total;
+        }
+        return ylast;
+    }
+};
+
 // Fixed-point sum (weights times `scale`) of the chunks [k0, k1) and their last positive
 // element, over the warp (every lane returns both).
 template <typename DQ, typename DP, int E, bool BONUS>

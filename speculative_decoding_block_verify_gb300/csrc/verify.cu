@@ -1382,6 +1382,53 @@ struct FinishShared {
     float seg[SPEC_MAX_KMAX + 1][kSegs];         // every slot's segment sums (swept slots hold data)
 };
 
+// The draw's last two steps over the drawn segment [s0, s1): every warp sums an eighth of it
+// in fixed point, and the warp whose eighth crosses the target rescans that eighth (from the
+// weights it already holds when the eighth is at most 64 chunks, else by reading it again).
+// The token is written to out_tok[slot_out] by the thread that found it.
+template <typename DQ, typename DP, int E, bool BONUS>
+__device__ __forceinline__ void draw_in_segment(const VerifyParams& p, FinishShared& sh, const void* rq, const void* rp,
+                                                int64_t s0, int64_t s1, float Kq, float Kp, float ah, float al,
+                                                float cc, int warp, int lane, int64_t slot_out) {
+    const int64_t msub = (s1 - s0 + kWarps - 1) / kWarps;
+    const int64_t w0 = min(s1, s0 + warp * msub), w1 = min(s1, w0 + msub);
+    const bool held = msub <= 64;
+    DrawSlice<DQ, DP, E, BONUS> slice;
+    unsigned long long sub;
+    int last;
+    if (held) {
+        slice.load(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, lane, p.t2d, p.Kq);
+        slice.sum(sub, last);
+    } else {
+        segment_fixed_sum<DQ, DP, E, BONUS>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, lane, sub, last,
+                                            p.t2d, p.Kq);
+    }
+    if (lane == 0) {
+        sh.sub_sum[warp] = sub;
+        sh.sub_last[warp] = last;
+    }
+    __syncthreads();
+    const unsigned long long t = sh.sample_t;
+    unsigned long long before = 0;
+    int wsel = -1, lastpos = -1;
+    for (int w = 0; w < kWarps; ++w) {
+        lastpos = max(lastpos, sh.sub_last[w]);
+        if (wsel < 0) {
+            if (sh.sub_sum[w] > 0 && before + sh.sub_sum[w] > t) wsel = w;
+            else before += sh.sub_sum[w];
+        }
+    }
+    int y = -1;
+    if (wsel < 0) {
+        y = lastpos;   // rounding kept the segment's sum at or below the target
+    } else if (warp == wsel) {
+        y = held ? slice.rescan(t - before, lane)
+                 : rescan_segment<DQ, DP, E, BONUS>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, t - before,
+                                                    lane, p.t2d, p.Kq);
+    }
+    if ((wsel < 0 && threadIdx.x == 0) || (warp == wsel && lane == 0)) p.out_tok[slot_out] = y;
+}
+
 template <typename DQ, typename DP, int E>
 __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) {
     __shared__ FinishShared sh;
@@ -1581,41 +1628,10 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) 
             const float cc = bonus ? 0.f : sh.cval[tau];
             const int64_t s0 = min(p.nchunk, (int64_t)sh.sample_seg * p.seg_chunks);
             const int64_t s1 = min(p.nchunk, s0 + p.seg_chunks);
-            const int64_t msub = (s1 - s0 + kWarps - 1) / kWarps;
-            const int64_t w0 = min(s1, s0 + warp * msub), w1 = min(s1, w0 + msub);
-            unsigned long long sub;
-            int last;
             if (bonus)
-                segment_fixed_sum<DQ, DP, E, true>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, lane, sub,
-                                                   last, p.t2d, p.Kq);
+                draw_in_segment<DQ, DP, E, true>(p, sh, rq, rp, s0, s1, Kq, Kp, ah, al, cc, warp, lane, ob + tau);
             else
-                segment_fixed_sum<DQ, DP, E, false>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale, lane, sub,
-                                                    last, p.t2d, p.Kq);
-            if (lane == 0) {
-                sh.sub_sum[warp] = sub;
-                sh.sub_last[warp] = last;
-            }
-            __syncthreads();
-            const unsigned long long t = sh.sample_t;
-            unsigned long long before = 0;
-            int wsel = -1, lastpos = -1;
-            for (int w = 0; w < kWarps; ++w) {
-                lastpos = max(lastpos, sh.sub_last[w]);
-                if (wsel < 0) {
-                    if (sh.sub_sum[w] > 0 && before + sh.sub_sum[w] > t) wsel = w;
-                    else before += sh.sub_sum[w];
-                }
-            }
-            int y = -1;
-            if (wsel < 0) {
-                y = lastpos;   // rounding kept the segment's sum at or below the target
-            } else if (warp == wsel) {
-                y = bonus ? rescan_segment<DQ, DP, E, true>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale,
-                                                            t - before, lane, p.t2d, p.Kq)
-                          : rescan_segment<DQ, DP, E, false>(rq, rp, w0, w1, Kq, Kp, ah, al, cc, sh.sample_scale,
-                                                             t - before, lane, p.t2d, p.Kq);
-            }
-            if ((wsel < 0 && tid == 0) || (warp == wsel && lane == 0)) p.out_tok[ob + tau] = y;
+                draw_in_segment<DQ, DP, E, false>(p, sh, rq, rp, s0, s1, Kq, Kp, ah, al, cc, warp, lane, ob + tau);
         }
     }
 
