@@ -12,7 +12,7 @@
 // vocabulary for the whole walk.  Per slot: the CTA gathers W1[t_{i-1}] of up to kWalkGroup
 // streams into shared memory and computes the biased logits of its slice - W2 (66 MB for rank
 // 256 at V = 129,280) is read once per slot for all streams of the group and stays in L2
-// between slots - writes them (they are the rows the verify's q is taken from) and publishes
+// between slots; the CTA's 8 warps split it as 4 column groups x 2 rank halves - writes them (they are the rows the verify's q is taken from) and publishes
 // one partial: (integer reference K, sum of 2^(l~ a - K)) for T > 0, (maximum, lowest index)
 // for T = 0.  After a grid barrier every CTA reduces the same partials in the same order, so
 // all agree on the draw: the 64-bit fixed-point CDF over the slices (the verify's scheme)
@@ -22,6 +22,8 @@
 // streams TIMEOUT.
 
 #include <cooperative_groups.h>
+
+#include <atomic>
 
 #include <cfloat>
 #include <climits>
@@ -173,45 +175,72 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                 mx[g] = -kInf;
                 arg[g] = INT_MAX;
             }
-            for (int64_t k = k0 + tid; k < k1; k += kWalkThreads) {
+            // The 8 warps take (32 chunks, half of the rank): warp w sums ranks
+            // [h R / 2, (h + 1) R / 2), h = w / 4, of chunks base + 32 (w % 4) + lane, a lane with 16
+            // W2 loads in flight; the upper half's sums meet the lower half's in shared memory,
+            // where the lower half's warps finish the chunks.
+            const int half = warp >> 2, cgrp = warp & 3;
+            const int jsplit = (p.R + 1) / 2;
+            const int ja = half ? jsplit : 0, jb = half ? p.R : jsplit;
+            float* red = w1s + kWalkGroup * p.R;   // [4][32][kWalkGroup][E]
+            for (int64_t cb = k0; cb < k1; cb += 4 * 32) {
+                const int64_t k = cb + cgrp * 32 + lane;
+                const bool act = k < k1;
                 float acc[kWalkGroup][E];
 #pragma unroll
                 for (int g = 0; g < kWalkGroup; ++g)
 #pragma unroll
                     for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
-#pragma unroll 4
-                for (int j = 0; j < p.R; ++j) {
-                    Chunk<WT, E> cwv;
-                    cwv.load(row_ptr<WT>(p.W2, j, V), k);
-                    float x[E];
-                    cwv.unpack(x);
+                if (act) {
+#pragma unroll 16
+                    for (int j = ja; j < jb; ++j) {
+                        Chunk<WT, E> cwv;
+                        cwv.load(row_ptr<WT>(p.W2, j, V), k);
+                        float x[E];
+                        cwv.unpack(x);
 #pragma unroll
-                    for (int g = 0; g < kWalkGroup; ++g) {
-                        const float wv = w1s[g * p.R + j];
+                        for (int g = 0; g < kWalkGroup; ++g) {
+                            const float wv = w1s[g * p.R + j];
 #pragma unroll
-                        for (int e = 0; e < E; ++e) acc[g][e] = fmaf(wv, x[e], acc[g][e]);
-                    }
-                }
-#pragma unroll
-                for (int g = 0; g < kWalkGroup; ++g) {
-                    if (g >= gn) continue;
-                    const int64_t row = ((int64_t)(g0 + g) * p.N + i);
-                    Chunk<DT, E> cd;
-                    cd.load(row_ptr<DT>(p.draft, row, V), k);
-                    float d[E];
-                    cd.unpack(d);
-                    float* o = p.out + row * V + k * E;
-#pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float l = s_alive[g] ? d[e] + acc[g][e] : qnan;
-                        o[e] = l;
-                        const float key = s_greedy[g] ? l : l * s_ah[g];
-                        if (!(key <= mx[g])) {   // a new maximum, NaN included (it then sticks)
-                            if (!(key == mx[g])) arg[g] = (int)(k * E + e);
-                            mx[g] = fmax_nan(mx[g], key);
+                            for (int e = 0; e < E; ++e) acc[g][e] = fmaf(wv, x[e], acc[g][e]);
                         }
                     }
                 }
+                float* rl = red + ((cgrp * 32 + lane) * kWalkGroup) * E;
+                if (half) {
+#pragma unroll
+                    for (int g = 0; g < kWalkGroup; ++g)
+#pragma unroll
+                        for (int e = 0; e < E; ++e) rl[g * E + e] = acc[g][e];
+                }
+                __syncthreads();   // the upper half's sums are in shared memory
+                if (!half && act) {
+#pragma unroll
+                    for (int g = 0; g < kWalkGroup; ++g)
+#pragma unroll
+                        for (int e = 0; e < E; ++e) acc[g][e] += rl[g * E + e];
+#pragma unroll
+                    for (int g = 0; g < kWalkGroup; ++g) {
+                        if (g >= gn) continue;
+                        const int64_t row = ((int64_t)(g0 + g) * p.N + i);
+                        Chunk<DT, E> cd;
+                        cd.load(row_ptr<DT>(p.draft, row, V), k);
+                        float d[E];
+                        cd.unpack(d);
+                        float* o = p.out + row * V + k * E;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) {
+                            const float l = s_alive[g] ? d[e] + acc[g][e] : qnan;
+                            o[e] = l;
+                            const float key = s_greedy[g] ? l : l * s_ah[g];
+                            if (!(key <= mx[g])) {   // a new maximum, NaN included (it then sticks)
+                                if (!(key == mx[g])) arg[g] = (int)(k * E + e);
+                                mx[g] = fmax_nan(mx[g], key);
+                            }
+                        }
+                    }
+                }
+                __syncthreads();   // the lower half is done with the shared sums
             }
             // CTA maximum (NaN-aware) and its lowest index, per stream
 #pragma unroll
@@ -439,19 +468,21 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
 
 template <typename DT, typename WT, int E>
 static cudaError_t launch_walk(WalkParams& p, cudaStream_t s) {
-    static int grid_cache[64] = {0};
+    static std::atomic<int> grid_cache[64];   // per device: the cooperative grid (0: not yet set up)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    const size_t smem = sizeof(float) * (size_t)kWalkGroup * p.R;
-    if (grid_cache[dev] == 0) {
+    const size_t red_bytes = sizeof(float) * 4 * 32 * kWalkGroup * E;   // the rank halves' meeting area
+    const size_t smem = sizeof(float) * (size_t)kWalkGroup * p.R + red_bytes;
+    int grid = grid_cache[dev].load(std::memory_order_acquire);
+    if (grid == 0) {
         cudaError_t e = cudaFuncSetAttribute(walk_kernel<DT, WT, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(sizeof(float) * kWalkGroup * kWalkMaxRank));
+                                             (int)(sizeof(float) * kWalkGroup * kWalkMaxRank + red_bytes));
         if (e != cudaSuccess) return e;
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
-        grid_cache[dev] = sms < kWalkMaxCtas ? sms : kWalkMaxCtas;
+        grid = sms < kWalkMaxCtas ? sms : kWalkMaxCtas;
+        grid_cache[dev].store(grid, std::memory_order_release);
     }
-    const int grid = grid_cache[dev];
     p.cw = (p.nchunk + grid - 1) / grid;
     // the barrier counter and timeout flag start at zero in every launch
     cudaError_t e = cudaMemsetAsync(p.ws, 0, 8, s);
