@@ -17,10 +17,12 @@
 // kernel 1): batch mode's ordering of all (stream, slot) entries and its pick, then the
 // exclusive prefix sum that gives cu_drafts.
 
+#include <atomic>
 #include <cfloat>
 #include <climits>
 
 #include "common.cuh"
+#include "df.cuh"
 #include "host_util.h"
 
 namespace sv {
@@ -162,80 +164,118 @@ __device__ void write_cu(const int32_t* k, int32_t* cu, int B) {
     if (tid == 0) cu[B] = carry;
 }
 
+// Batch mode's ordering as a bitonic sort of 64-bit keys in shared memory: key = (~bits of
+// a) << 32 | entry, entry = b kmax + j.  Sorting the keys ascending orders a descending (a is
+// in [0, 1], where the float bits are monotone) and equal a by (stream, slot) ascending, the
+// order the pages' scheduler adds candidates in.  Padding keys (all ones) sort last.
+__device__ __forceinline__ float key_a(unsigned long long key) { return __uint_as_float(~(uint32_t)(key >> 32)); }
+__device__ __forceinline__ int key_entry(unsigned long long key) { return (int)(uint32_t)key; }
+
 __global__ void __launch_bounds__(kPickThreads) pick_batch_kernel(const PickParams p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");   // every confidence CTA has finished
-    __shared__ float a_s[kMaxBatchEntries];
-    __shared__ uint16_t order[kMaxBatchEntries];   // order[rank] = entry
-    __shared__ int k_s[kMaxBatchEntries];
-    __shared__ double best_v[kPickThreads / 32];
+    extern __shared__ __align__(16) unsigned long long keys[];   // [npow2], then k_s [B] int
+    __shared__ df best_v[kPickThreads / 32];
     __shared__ int best_m[kPickThreads / 32];
-    __shared__ double seg_tot[kPickThreads / 32];
+    __shared__ df seg_tot[kPickThreads / 32];
+    __shared__ df seg_ofs[kPickThreads / 32];
     __shared__ int m_star;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = p.B * p.kmax;
     if (p.mode == 1) {
-        for (int e = tid; e < n; e += kPickThreads) a_s[e] = p.a_out[e];
+        int npow2 = 1;
+        while (npow2 < n) npow2 <<= 1;
+        int* k_s = reinterpret_cast<int*>(keys + npow2);
+        for (int e = tid; e < npow2; e += kPickThreads)
+            keys[e] = e < n ? ((unsigned long long)(~__float_as_uint(p.a_out[e])) << 32) | (unsigned)e : ~0ull;
         for (int b = tid; b < p.B; b += kPickThreads) k_s[b] = 0;
         __syncthreads();
-        // rank of entry e under (a desc, stream asc, slot asc); entry index = b * kmax + j
-        // already orders (stream, slot), so ties in a break by the entry index.
-        for (int e = tid; e < n; e += kPickThreads) {
-            const float ae = a_s[e];
-            int rank = 0;
-            for (int f = 0; f < n; ++f) {
-                const float af = a_s[f];
-                rank += (af > ae) || (af == ae && f < e);
+        for (int kk = 2; kk <= npow2; kk <<= 1)
+            for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+                for (int i = tid; i < npow2; i += kPickThreads) {
+                    const int ixj = i ^ jj;
+                    if (ixj > i) {
+                        const unsigned long long x = keys[i], y = keys[ixj];
+                        if ((x > y) == ((i & kk) == 0)) {
+                            keys[i] = y;
+                            keys[ixj] = x;
+                        }
+                    }
+                }
+                __syncthreads();
             }
-            order[rank] = e;
-        }
-        __syncthreads();
-        // S_m for m = 1..n: each thread owns a contiguous run of ranks
+        // S_m for m = 1..n: each thread owns a contiguous run of ranks.  Double-float scalars
+        // (~48 bits; this part's float64 pipe is narrow): the run sums, one scan across the lanes,
+        // one across the warps' totals, then every m's ratio (B + S_m) / verify_ms[B + m].
         const int per = (n + kPickThreads - 1) / kPickThreads;
-        const int m0 = tid * per, m1 = min(n, m0 + per);
-        double run = 0.0;
-        for (int m = m0; m < m1; ++m) run += (double)a_s[order[m]];
-        // exclusive scan of the runs (warp, then block)
-        double incl = run;
+        const int m0 = min(n, tid * per), m1 = min(n, m0 + per);
+        df run{0.f, 0.f};
+        for (int m = m0; m < m1; ++m) run = df_add_f(run, key_a(keys[m]));
+        df incl = run;   // inclusive scan of the runs across the warp
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const double nb = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += nb;
+            const df nb{__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
+            if (lane >= o) incl = df_add(incl, nb);
         }
         if (lane == 31) seg_tot[warp] = incl;
         __syncthreads();
-        double wofs = 0.0;
-        for (int w = 0; w < warp; ++w) wofs += seg_tot[w];
-        double s = wofs + incl - run;   // sum of the ranks before m0
-        // best ratio over this thread's m (m = number chosen, 1-based) ; m = 0 handled below
-        double bv = -1.0;
+        if (warp == 0) {   // exclusive scan of the warps' totals
+            df t = lane < kPickThreads / 32 ? seg_tot[lane] : df{0.f, 0.f};
+            df inc = t;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const df nb{__shfl_up_sync(0xffffffffu, inc.hi, o), __shfl_up_sync(0xffffffffu, inc.lo, o)};
+                if (lane >= o) inc = df_add(inc, nb);
+            }
+            if (lane < kPickThreads / 32) seg_ofs[lane] = df_sub(inc, t);
+        }
+        __syncthreads();
+        df sm = df_sub(df_add(seg_ofs[warp], incl), run);   // the sum of the ranks before m0
+        // best ratio over this thread's m (m = number chosen, 1-based); m = 0 handled below
+        df bv{-1.f, 0.f};
         int bm = INT_MAX;
+        const df Bd = df_make((float)p.B);
         for (int m = m0; m < m1; ++m) {
-            s += (double)a_s[order[m]];
-            const double v = ((double)p.B + s) / (double)p.verify_ms[p.B + m + 1];
-            if (v > bv) { bv = v; bm = m + 1; }
+            sm = df_add_f(sm, key_a(keys[m]));
+            const df v = df_div(df_add(Bd, sm), df_make(p.verify_ms[p.B + m + 1]));
+            if (df_lt(bv, v)) {
+                bv = v;
+                bm = m + 1;
+            }
         }
         if (tid == 0) {
-            const double v0 = (double)p.B / (double)p.verify_ms[p.B];
-            if (!(bv > v0)) { bv = v0; bm = 0; }   // ties go to the smaller m
+            const df v0 = df_div(Bd, df_make(p.verify_ms[p.B]));
+            if (!df_lt(v0, bv)) {   // ties go to the smaller m
+                bv = v0;
+                bm = 0;
+            }
         }
         // block argmax (larger value, then smaller m)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const df ov{__shfl_xor_sync(0xffffffffu, bv.hi, o), __shfl_xor_sync(0xffffffffu, bv.lo, o)};
             const int om = __shfl_xor_sync(0xffffffffu, bm, o);
-            if (ov > bv || (ov == bv && om < bm)) { bv = ov; bm = om; }
+            if (df_lt(bv, ov) || (!df_lt(ov, bv) && om < bm)) {
+                bv = ov;
+                bm = om;
+            }
         }
-        if (lane == 0) { best_v[warp] = bv; best_m[warp] = bm; }
+        if (lane == 0) {
+            best_v[warp] = bv;
+            best_m[warp] = bm;
+        }
         __syncthreads();
         if (tid == 0) {
-            double v = best_v[0];
+            df v = best_v[0];
             int m = best_m[0];
             for (int w = 1; w < kPickThreads / 32; ++w)
-                if (best_v[w] > v || (best_v[w] == v && best_m[w] < m)) { v = best_v[w]; m = best_m[w]; }
+                if (df_lt(v, best_v[w]) || (!df_lt(best_v[w], v) && best_m[w] < m)) {
+                    v = best_v[w];
+                    m = best_m[w];
+                }
             m_star = m;
         }
         __syncthreads();
-        for (int r = tid; r < m_star; r += kPickThreads) atomicAdd(&k_s[order[r] / p.kmax], 1);
+        for (int r = tid; r < m_star; r += kPickThreads) atomicAdd(&k_s[key_entry(keys[r]) / p.kmax], 1);
         __syncthreads();
         for (int b = tid; b < p.B; b += kPickThreads) p.k_out[b] = k_s[b];
         __syncthreads();
@@ -252,9 +292,26 @@ static cudaError_t launch_pick(PickParams p, cudaStream_t s) {
     confidence_kernel<T, E><<<p.B, kConfWarps * 32, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    size_t smem = 0;
+    if (p.mode == 1) {   // the sort keys and the per-stream counts
+        int npow2 = 1;
+        while (npow2 < p.B * p.kmax) npow2 <<= 1;
+        smem = (size_t)npow2 * sizeof(unsigned long long) + (size_t)p.B * sizeof(int);
+        static std::atomic<int> attr_set[64];
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
+            e = cudaFuncSetAttribute(pick_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kMaxBatchEntries * (sizeof(unsigned long long) + sizeof(int))));
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) attr_set[dev].store(1, std::memory_order_release);
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1);
     cfg.blockDim = dim3(kPickThreads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
