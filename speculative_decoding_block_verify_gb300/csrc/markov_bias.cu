@@ -414,8 +414,10 @@ __global__ void __launch_bounds__(kBiasThreads, 2) markov_bias_mma_kernel(const 
     const int r0 = blockIdx.y * kMmaRows;
     const int nr = min(kMmaRows, p.rows - r0);
     const int nkb = Rp / KB;
+    // strip s goes to warp s / gridDim.x of CTA s % gridDim.x (then every W-th): with the grid at
+    // the resident CTA count, the CTAs sharing an SM get strip counts that differ by at most one
     const int W = gridDim.x * kBiasWarps;
-    const int s_first = blockIdx.x * kBiasWarps + warp;
+    const int s_first = blockIdx.x + warp * gridDim.x;
     const int nmine = s_first < nstrips ? (nstrips - s_first + W - 1) / W : 0;
     const int total = nmine * nkb;   // boxes this warp streams: its strips in order, each over all ranks
     char* ring = base + warp * kMmaStages * kMmaBoxBytes;
@@ -686,8 +688,7 @@ static cudaError_t launch_bias_mma(const BiasParams& p, cudaStream_t s, bool* un
         if (dev >= 0 && dev < 64) MmaAttr<DT>::grid[dev].store(resident, std::memory_order_release);
     }
     const int nstrips = (int)((p.V + kMmaCols - 1) / kMmaCols);
-    const int need = (nstrips + kBiasWarps - 1) / kBiasWarps;
-    const dim3 grid((unsigned)(need < resident ? need : resident), (unsigned)((p.rows + kMmaRows - 1) / kMmaRows));
+    const dim3 grid((unsigned)(nstrips < resident ? nstrips : resident), (unsigned)((p.rows + kMmaRows - 1) / kMmaRows));
     markov_bias_mma_kernel<DT><<<grid, kBiasThreads, mma_smem_bytes(p.R), s>>>(p, map, nstrips);
     return cudaGetLastError();
 }
