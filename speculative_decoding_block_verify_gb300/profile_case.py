@@ -13,7 +13,8 @@ calls; nothing is timed or checked here - bench.py and the tests do that):
   bias_single              dspark_markov_bias, 5 rows, rank 256, V = 129,280, bf16, with a
                            256 MB scrub before every call so that W2 is read from HBM
   walk_single              dspark_markov_walk, one stream, N = 5, rank 256, V = 129,280, bf16
-  pick_adaptive128         adaptive_pick_k, B = 128, kmax = 5, H = 7168, bf16
+  pick_adaptive128         adaptive_pick_k, B = 128, kmax = 5, H = 7168, bf16, per-stream mode
+  pick_batch_adaptive128   the same in batch mode (the sort of the entries in pick_batch_kernel)
   pipeline_adaptive128     SpecPipeline.launch (pick -> verify -> counters -> step + 1)
 
 A profiler filters the launches it captures by kernel name and skips the warm-up calls.
@@ -76,14 +77,15 @@ def main(argv=None):
             out = None
             for i in range(total):
                 out = sv.dspark_markov_walk(dq.view(1, 5, -1), prev[:1].contiguous(), w1, w2, T, 0, i, out=out)
-    elif a.case in ("pick_adaptive128", "pipeline_adaptive128"):
+    elif a.case in ("pick_adaptive128", "pick_batch_adaptive128", "pipeline_adaptive128"):
         c = workloads.make_confidence_inputs(12)
         h, w = _bf(torch, c["hidden"], dev), _bf(torch, c["w"], dev)
         vm = torch.as_tensor(c["verify_ms"], device=dev)
-        if a.case == "pick_adaptive128":
+        if a.case != "pipeline_adaptive128":
             pk = None
+            mode = 1 if a.case == "pick_batch_adaptive128" else 0
             for _ in range(total):
-                pk = sv.adaptive_pick_k(h, w, 0.0, vm, out=pk)
+                pk = sv.adaptive_pick_k(h, w, 0.0, vm, mode=mode, out=pk)
         else:
             dn = workloads.make_verify_inputs("adaptive128", 13, backend="torch", device=dev)
             B, K, V = 128, 5, dn["V"]
