@@ -189,7 +189,7 @@ typedef struct {
 /*
  * spec_verify_workspace_bytes - device workspace a verify call over B streams with up to
  * kmax drafts each needs (16-byte aligned, caller-allocated; 0 for B = 0 and for invalid
- * arguments): 256 + 1536 B (2 kmax + 1) + 1024 B (kmax + 1) bytes.  It holds the claim tickets
+ * arguments): 256 + 1536 B (2 kmax + 1) + 2048 B (kmax + 1) bytes.  It holds the claim tickets
  * of the two persistent kernels, per row the statistics partials and a counter of the pieces
  * published, the per-slot and per-stream scalars that one kernel of the call hands to the
  * next, and the residual sweep's work list.  Zero-fill it once before the first call; every

@@ -46,8 +46,10 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxRows = 2 * SPEC_MAX_KMAX + 1;
 constexpr float kNoRef = -1e30f;     // reference of a lane that has seen no finite logit
 constexpr int kSegs = 64;            // residual segments per row: the draw's CDF resolution
+constexpr int kSegLanes = kSegs / 32;   // segments a lane holds in the per-row warp steps
+static_assert(kSegs % 32 == 0, "segments come in whole warps");
 constexpr int kPiecesMax = 64;       // stats partials per row
-constexpr int kSegsPerClaim = 2;     // a sweep claim spans 2 segments of one row pair
+constexpr int kSegsPerClaim = 1;     // a sweep claim is one segment of one row pair (2 took 2 us more: coarser balance)
 constexpr int kStatsThreads = 256;   // threads of a stats CTA
 constexpr int kStatsWarps = kStatsThreads / 32;
 
@@ -635,15 +637,16 @@ __device__ __forceinline__ int stream_of_row(const VerifyParams& p, int64_t rho,
 // warp; the remaining rows in fixed pieces of two segments, claimed by whichever warp is free
 // (so SMs that run slower, or whose CTAs started later, simply take fewer of them).  The claimed
 // tail pays a ramp and a claim per piece, which only a long share amortises: measured on the
-// batch-64 bf16 call (~50 KB per warp) any tail costs more than the end-time spread it removes,
-// on the batch-256 fp32 call (~690 KB per warp) a fifth of the rows as tail saves ~10%.  So the
-// tail is a fifth of the rows when a warp's share is at least kTailMinChunks chunks, else empty.
+// batch-64 bf16 call (~75 KB per warp) a twentieth, a tenth or a fifth of the rows as tail cost
+// 4, 6 and 9 us more than none (75 us); on the batch-256 fp32 call (~1 MB per warp) a tenth
+// takes 510 us, a twentieth 516 us, a fifth 533 us.  So the tail is a tenth of the rows when a
+// warp's share is at least kTailMinChunks chunks, else empty.
 // Draft rows over a reduced draft vocabulary are shorter than target rows; their calls take
 // every row static (the tail's fixed pieces assume one row length).
 constexpr int64_t kTailMinChunks = 16384;
 __host__ __device__ inline int64_t static_rows(int64_t rows, int64_t n, int64_t warps, bool reduced) {
     if (reduced) return rows;
-    return (rows * n >= kTailMinChunks * warps) ? rows * 4 / 5 : rows;
+    return (rows * n >= kTailMinChunks * warps) ? rows * 9 / 10 : rows;
 }
 __host__ __device__ inline int64_t tail_pieces_per_row(int64_t n, int64_t seg_chunks) {
     const int64_t pc = 2 * seg_chunks;
@@ -1538,7 +1541,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) 
             const int i = sh.pass_list[it];
             df tot{0.f, 0.f};
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
+            for (int k = 0; k < kSegLanes; ++k) {
                 const int sg = lane + 32 * k;
                 tot = df_add_f(tot, sg < p.nseg ? sh.seg[i][sg] : 0.f);
             }
@@ -1570,42 +1573,53 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyParams p) 
         }
         __syncthreads();
 
-        // ---- the draw: 64-bit fixed-point CDF over the drawn item's segments (warp 0)
+        // ---- the draw: 64-bit fixed-point CDF over the drawn item's segments (warp 0); lane l
+        // holds segments l, l + 32, ...: the scan runs block by block, each block's inclusive
+        // prefix plus the total of the blocks before it
         if (warp == 0) {
             const int tau = sh.tau;
-            const float w0 = lane < p.nseg ? sh.seg[tau][lane] : 0.f;
-            const float w1 = lane + 32 < p.nseg ? sh.seg[tau][lane + 32] : 0.f;
-            const float wmax = warp_max(fmaxf(w0, w1));
+            float wv[kSegLanes];
+            float wm = 0.f;
+#pragma unroll
+            for (int k = 0; k < kSegLanes; ++k) {
+                const int sg = lane + 32 * k;
+                wv[k] = sg < p.nseg ? sh.seg[tau][sg] : 0.f;
+                wm = fmaxf(wm, wv[k]);
+            }
+            const float wmax = warp_max(wm);
             const bool ok = isfinite(wmax) && wmax > 0.f;
             const float scale = ok ? fixed_scale(wmax) : 0.f;
-            const unsigned long long q0 = ok ? __float2ull_rn(w0 * scale) : 0ull;
-            const unsigned long long q1 = ok ? __float2ull_rn(w1 * scale) : 0ull;
-            unsigned long long p0 = q0, p1 = q1;   // inclusive prefix sums
+            unsigned long long q[kSegLanes], pre[kSegLanes];   // weights, inclusive prefix sums
+            unsigned long long carry = 0;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long n0 = __shfl_up_sync(0xffffffffu, p0, o);
-                const unsigned long long n1 = __shfl_up_sync(0xffffffffu, p1, o);
-                if (lane >= o) {
-                    p0 += n0;
-                    p1 += n1;
+            for (int k = 0; k < kSegLanes; ++k) {
+                q[k] = ok ? __float2ull_rn(wv[k] * scale) : 0ull;
+                unsigned long long v = q[k];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long n = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += n;
                 }
+                pre[k] = v + carry;
+                carry = __shfl_sync(0xffffffffu, pre[k], 31);
             }
-            p1 += __shfl_sync(0xffffffffu, p0, 31);
-            const unsigned long long R = __shfl_sync(0xffffffffu, p1, 31);
+            const unsigned long long R = carry;
             // t = floor(U R), U = (2k + 1) 2^-25 with k the word's top 24 bits
             const unsigned long long odd = 2ull * (sh.u_smp[tau] >> 8) + 1ull;
             const unsigned long long t = (__umul64hi(odd, R) << 39) | ((odd * R) >> 25);
-            const unsigned h0 = __ballot_sync(0xffffffffu, q0 > 0 && p0 > t);
-            const unsigned h1 = __ballot_sync(0xffffffffu, q1 > 0 && p1 > t);
-            const int sg = h0 ? __ffs(h0) - 1 : (h1 ? 32 + __ffs(h1) - 1 : -1);
-            const int src = sg < 0 ? 0 : sg % 32;
-            const unsigned long long i0 = __shfl_sync(0xffffffffu, p0, src);
-            const unsigned long long i1 = __shfl_sync(0xffffffffu, p1, src);
-            const unsigned long long qs0 = __shfl_sync(0xffffffffu, q0, src);
-            const unsigned long long qs1 = __shfl_sync(0xffffffffu, q1, src);
+            int sg = -1;
+            unsigned long long excl = 0;
+#pragma unroll
+            for (int k = 0; k < kSegLanes; ++k) {
+                const unsigned hit = __ballot_sync(0xffffffffu, q[k] > 0 && pre[k] > t);
+                if (sg < 0 && hit) {
+                    const int src = __ffs(hit) - 1;
+                    sg = 32 * k + src;
+                    excl = __shfl_sync(0xffffffffu, pre[k] - q[k], src);
+                }
+            }
             if (lane == 0) {
                 if (ok && R > 0 && sg >= 0) {
-                    const unsigned long long excl = (sg < 32) ? i0 - qs0 : i1 - qs1;
                     sh.sample_t = t - excl;
                     sh.sample_scale = scale;
                     sh.sample_seg = sg;

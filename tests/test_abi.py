@@ -89,9 +89,9 @@ def test_workspace_size_and_check(L):
     # one block per row: a 16-byte counter slot and 64 partials of 16 bytes
     # a 256-byte header, a 1536-byte block per stats row (at the same offset for every B and
     # kmax), then the residual sweep's work list: 32 bytes per claim, 32 claims per slot
-    assert sv.spec_verify_workspace_bytes(64, 5) == 256 + 64 * 11 * 1536 + 64 * 6 * 32 * 32
+    assert sv.spec_verify_workspace_bytes(64, 5) == 256 + 64 * 11 * 1536 + 64 * 6 * 64 * 32
     for B, kmax in ((1, 0), (7, 3), (256, 15), (3, 32)):
-        assert sv.spec_verify_workspace_bytes(B, kmax) == 256 + B * (2 * kmax + 1) * 1536 + B * (kmax + 1) * 1024
+        assert sv.spec_verify_workspace_bytes(B, kmax) == 256 + B * (2 * kmax + 1) * 1536 + B * (kmax + 1) * 2048
     assert sv.spec_verify_workspace_bytes(0, 5) == 0
     assert sv.spec_verify_workspace_bytes(-1, 5) == 0
     assert sv.spec_verify_workspace_bytes(4, 33) == 0
