@@ -105,9 +105,17 @@ __device__ bool walk_barrier(unsigned* ctr, unsigned* timed_out, unsigned target
     return ok != 0;
 }
 
+// Dynamic shared memory of a walk CTA: the group's W1 rows [kWalkGroup][R] floats, the rank
+// halves' meeting area [4][32][kWalkGroup][E] floats, then (16-byte aligned) one float4 per CTA
+// of the grid for the partials of the stream being drawn.
+__host__ __device__ inline size_t walk_parts_offset(int R, int E) {
+    const size_t b = sizeof(float) * ((size_t)kWalkGroup * R + (size_t)4 * 32 * kWalkGroup * E);
+    return (b + 15) & ~(size_t)15;
+}
+
 template <typename DT, typename WT, int E>
 __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams p) {
-    extern __shared__ float w1s[];   // [kWalkGroup][R], then the reduction area
+    extern __shared__ __align__(16) float w1s[];   // [kWalkGroup][R], the reduction area, the CTAs' partials
     __shared__ int s_prev[kWalkGroup], s_alive[kWalkGroup], s_greedy[kWalkGroup], s_status[kWalkGroup];
     __shared__ float s_ah[kWalkGroup], s_al[kWalkGroup];
     __shared__ float s_red[kWalkWarps][kWalkGroup][4];
@@ -122,6 +130,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
     unsigned* ctr = reinterpret_cast<unsigned*>(p.ws);
     unsigned* timed_out = ctr + 1;
     WalkPart* parts = reinterpret_cast<WalkPart*>(p.ws + 256);
+    // one stream's partials of every CTA, read from L2 once per draw by warp 0
+    float4* s_parts = reinterpret_cast<float4*>(reinterpret_cast<char*>(w1s) + walk_parts_offset(p.R, E));
     unsigned target = 0;
     bool live = true;   // no barrier has given up
     const float qnan = __int_as_float(0x7fffffff);
@@ -319,12 +329,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                 const WalkPart* pb = parts + (int64_t)b * kWalkMaxCtas;
                 if (s_greedy[g]) {
                     if (warp == 0) {
+                        for (int q = lane; q < ncta; q += 32) s_parts[q] = __ldcg(reinterpret_cast<const float4*>(pb + q));
+                        __syncwarp();
                         float m = -kInf;
-                        for (int q = lane; q < ncta; q += 32) m = fmax_nan(m, __ldcg(&pb[q].K));
+                        for (int q = lane; q < ncta; q += 32) m = fmax_nan(m, s_parts[q].x);
                         m = warp_max_nan(m);
                         int a = INT_MAX;
                         for (int q = lane; q < ncta; q += 32)
-                            if (__ldcg(&pb[q].K) == m) a = min(a, __ldcg(&pb[q].idx));
+                            if (s_parts[q].x == m) a = min(a, __float_as_int(s_parts[q].w));
                         a = warp_min_i(a);
                         if (lane == 0) {
                             const bool bad = !isfinite(m) || a == INT_MAX;
@@ -339,10 +351,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                 }
                 // global reference and the slices' weights in 64-bit fixed point (warp 0)
                 if (warp == 0) {
+                    for (int q = lane; q < ncta; q += 32) s_parts[q] = __ldcg(reinterpret_cast<const float4*>(pb + q));
+                    __syncwarp();
                     float K = kWalkNoRef;
                     bool bad = false;
                     for (int q = lane; q < ncta; q += 32) {
-                        const float kq = __ldcg(&pb[q].K);
+                        const float kq = s_parts[q].x;
                         bad |= isnan(kq);
                         K = fmaxf(K, kq);
                     }
@@ -350,7 +364,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                     bad = __any_sync(0xffffffffu, bad) || !(K > kWalkNoRef) || !isfinite(K);
                     float wmax = 0.f;
                     for (int q = lane; q < ncta; q += 32) {
-                        const float4 e = __ldcg(reinterpret_cast<const float4*>(pb + q));
+                        const float4 e = s_parts[q];
                         const float wq = (e.y + e.z) * (e.x == K ? 1.f : pow2_int(e.x - K));
                         bad |= !isfinite(wq);
                         wmax = fmaxf(wmax, wq);
@@ -361,7 +375,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                     // total, then the first slice whose running sum passes t = floor(U R)
                     unsigned long long tot = 0;
                     for (int q = lane; q < ncta; q += 32) {
-                        const float4 e = __ldcg(reinterpret_cast<const float4*>(pb + q));
+                        const float4 e = s_parts[q];
                         tot += __float2ull_rn((e.y + e.z) * (e.x == K ? 1.f : pow2_int(e.x - K)) * scale);
                     }
 #pragma unroll
@@ -378,7 +392,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                         const int q = q0 + lane;
                         unsigned long long wq = 0;
                         if (q < ncta) {
-                            const float4 e = __ldcg(reinterpret_cast<const float4*>(pb + q));
+                            const float4 e = s_parts[q];
                             wq = __float2ull_rn((e.y + e.z) * (e.x == K ? 1.f : pow2_int(e.x - K)) * scale);
                         }
                         unsigned long long incl = wq;
@@ -471,12 +485,10 @@ static cudaError_t launch_walk(WalkParams& p, cudaStream_t s) {
     static std::atomic<int> grid_cache[64];   // per device: the cooperative grid (0: not yet set up)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    const size_t red_bytes = sizeof(float) * 4 * 32 * kWalkGroup * E;   // the rank halves' meeting area
-    const size_t smem = sizeof(float) * (size_t)kWalkGroup * p.R + red_bytes;
     int grid = grid_cache[dev].load(std::memory_order_acquire);
     if (grid == 0) {
         cudaError_t e = cudaFuncSetAttribute(walk_kernel<DT, WT, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(sizeof(float) * kWalkGroup * kWalkMaxRank + red_bytes));
+                                             (int)(walk_parts_offset(kWalkMaxRank, E) + sizeof(float4) * kWalkMaxCtas));
         if (e != cudaSuccess) return e;
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
@@ -484,6 +496,7 @@ static cudaError_t launch_walk(WalkParams& p, cudaStream_t s) {
         grid_cache[dev].store(grid, std::memory_order_release);
     }
     p.cw = (p.nchunk + grid - 1) / grid;
+    const size_t smem = walk_parts_offset(p.R, E) + sizeof(float4) * (size_t)grid;
     // the barrier counter and timeout flag start at zero in every launch
     cudaError_t e = cudaMemsetAsync(p.ws, 0, 8, s);
     if (e != cudaSuccess) return e;
