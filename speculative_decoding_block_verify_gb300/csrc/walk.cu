@@ -16,10 +16,11 @@
 // one partial: (integer reference K, sum of 2^(l~ a - K)) for T > 0, (maximum, lowest index)
 // for T = 0.  After a grid barrier every CTA reduces the same partials in the same order, so
 // all agree on the draw: the 64-bit fixed-point CDF over the slices (the verify's scheme)
-// picks the slice, and the CTA that owns it splits it over its warps and rescans one eighth.
-// It publishes t_i, and a second barrier releases the next slot.  The barriers are bounded
-// spins (a cooperative launch keeps every CTA resident); one that gives up makes the walk's
-// streams TIMEOUT.
+// picks the slice, and every CTA splits that slice over its warps and rescans one eighth, so
+// every CTA holds t_i for the next slot without a second barrier (CTA 0 publishes it; the
+// partials alternate between two buffers from slot to slot).  The barrier is a bounded spin
+// (a cooperative launch keeps every CTA resident); one that gives up makes the walk's streams
+// TIMEOUT.
 
 #include <cooperative_groups.h>
 
@@ -53,7 +54,7 @@ struct WalkParams {
     int32_t* tokens;       // [B, N]
     float* out;            // [B, N, V]
     int32_t* status;       // [B]
-    char* ws;              // workspace: barrier counter, timeout flag, partials [B][kWalkMaxCtas]
+    char* ws;              // workspace: barrier counter, timeout flag, partials [2][B][kWalkMaxCtas]
     int32_t B, N, V, R;
     int64_t nchunk;        // chunks of E elements per row
     int64_t cw;            // chunks per CTA slice
@@ -65,8 +66,11 @@ struct WalkPart {
     int idx;
 };
 
+// The barrier counter and timeout flag, then the CTAs' partials in two buffers: slot i writes
+// and reads buffer i mod 2, so a CTA already on slot i + 1 never overwrites partials that a
+// slower CTA is still reading for slot i's draw.
 __host__ __device__ inline size_t walk_workspace_bytes(int32_t B) {
-    return 256 + (size_t)B * kWalkMaxCtas * sizeof(WalkPart);
+    return 256 + 2 * (size_t)B * kWalkMaxCtas * sizeof(WalkPart);
 }
 
 __device__ __forceinline__ unsigned walk_now_load(const unsigned* p) {
@@ -120,6 +124,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
     __shared__ float s_ah[kWalkGroup], s_al[kWalkGroup];
     __shared__ float s_red[kWalkWarps][kWalkGroup][4];
     __shared__ int s_draw_seg;
+    __shared__ int s_tok[kWalkGroup];   // the token each stream of the group drew at the current slot
     __shared__ unsigned long long s_sub[kWalkWarps], s_t, s_excl;
     __shared__ int s_sub_last[kWalkWarps];
     __shared__ float s_scale, s_K;
@@ -168,8 +173,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
             if (tid < kWalkGroup) {
                 const int b = g0 + tid;
                 if (c == 0 && tid < gn && !s_alive[tid]) p.tokens[(int64_t)b * p.N + i] = -1;
-                s_prev[tid] = (s_alive[tid] != 0) ? (i == 0 ? p.anchor[b] : __ldcg(p.tokens + (int64_t)b * p.N + i - 1))
-                                                  : 0;
+                s_prev[tid] = (s_alive[tid] != 0) ? (i == 0 ? p.anchor[b] : s_tok[tid]) : 0;
             }
             __syncthreads();
             for (int t = tid; t < kWalkGroup * p.R; t += kWalkThreads) {
@@ -315,18 +319,20 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                 for (int w = 0; w < kWalkWarps; ++w) z = df_add(z, df{s_red[w][tid][0], s_red[w][tid][1]});
                 const int b = g0 + tid;
                 const bool gr = s_greedy[tid] != 0;
-                parts[(int64_t)b * kWalkMaxCtas + c] =
+                parts[((int64_t)(i & 1) * p.B + b) * kWalkMaxCtas + c] =
                     WalkPart{gr ? s_red[0][tid][2] : kref[tid], gr ? 0.f : z.hi, gr ? 0.f : z.lo,
                              gr ? __float_as_int(s_red[0][tid][3]) : INT_MAX};
             }
             live = live && walk_barrier(ctr, timed_out, target += ncta);
 
-            // ---- the draw, stream by stream (every CTA reduces the same partials in the same
-            // order, so all agree on the drawn slice; its owner rescans it)
+            // ---- the draw, stream by stream.  Every CTA reduces the same partials in the same
+            // order and rescans the same drawn slice of the biased row (in L2 since the barrier),
+            // so every CTA arrives at the same token, keeps it for the next slot's W1 row, and no
+            // second barrier is needed.
             for (int g = 0; g < gn; ++g) {
                 const int b = g0 + g;
                 if (!s_alive[g]) continue;
-                const WalkPart* pb = parts + (int64_t)b * kWalkMaxCtas;
+                const WalkPart* pb = parts + ((int64_t)(i & 1) * p.B + b) * kWalkMaxCtas;
                 if (s_greedy[g]) {
                     if (warp == 0) {
                         for (int q = lane; q < ncta; q += 32) s_parts[q] = __ldcg(reinterpret_cast<const float4*>(pb + q));
@@ -342,6 +348,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                             const bool bad = !isfinite(m) || a == INT_MAX;
                             if (bad) s_status[g] = SPEC_ST_BAD_ROW;
                             if (c == 0) p.tokens[(int64_t)b * p.N + i] = bad ? -1 : a;
+                            s_tok[g] = bad ? -1 : a;
                         }
                     }
                     __syncthreads();
@@ -434,14 +441,23 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                     __syncthreads();
                     continue;
                 }
-                if (s_draw_seg == c) {   // this CTA's slice holds the draw: split over the warps
+                {   // the drawn slice (CTA s_draw_seg's), split over the warps
                     const float* row = p.out + ((int64_t)b * p.N + i) * V;
-                    const int64_t msub = (k1 - k0 + kWalkWarps - 1) / kWalkWarps;
-                    const int64_t w0 = min(k1, k0 + warp * msub), w1 = min(k1, w0 + msub);
+                    const int64_t d0 = min(p.nchunk, (int64_t)s_draw_seg * p.cw), d1 = min(p.nchunk, d0 + p.cw);
+                    const int64_t msub = (d1 - d0 + kWalkWarps - 1) / kWalkWarps;
+                    const int64_t w0 = min(d1, d0 + warp * msub), w1 = min(d1, w0 + msub);
                     unsigned long long sub;
                     int last;
-                    segment_fixed_sum<float, f32_coherent, E, true>(nullptr, row, w0, w1, 0.f, s_K, s_ah[g], s_al[g],
-                                                                    0.f, s_scale, lane, sub, last, nullptr, 0);
+                    // an eighth of at most 64 chunks stays in registers between its sum and its rescan
+                    const bool held = msub <= 64;
+                    DrawSlice<float, f32_coherent, E, true> slice;
+                    if (held) {
+                        slice.load(nullptr, row, w0, w1, 0.f, s_K, s_ah[g], s_al[g], 0.f, s_scale, lane, nullptr, 0);
+                        slice.sum(sub, last);
+                    } else {
+                        segment_fixed_sum<float, f32_coherent, E, true>(nullptr, row, w0, w1, 0.f, s_K, s_ah[g], s_al[g],
+                                                                        0.f, s_scale, lane, sub, last, nullptr, 0);
+                    }
                     if (lane == 0) {
                         s_sub[warp] = sub;
                         s_sub_last[warp] = last;
@@ -460,13 +476,17 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                     int y = -1;
                     if (wsel < 0) y = lastpos;   // rounding kept the slice's sum at or below the target
                     else if (warp == wsel)
-                        y = rescan_segment<float, f32_coherent, E, true>(nullptr, row, w0, w1, 0.f, s_K, s_ah[g],
-                                                                         s_al[g], 0.f, s_scale, tt - bef, lane, nullptr, 0);
-                    if ((wsel < 0 && tid == 0) || (warp == wsel && lane == 0)) p.tokens[(int64_t)b * p.N + i] = y;
+                        y = held ? slice.rescan(tt - bef, lane)
+                                 : rescan_segment<float, f32_coherent, E, true>(nullptr, row, w0, w1, 0.f, s_K, s_ah[g],
+                                                                                s_al[g], 0.f, s_scale, tt - bef, lane,
+                                                                                nullptr, 0);
+                    if ((wsel < 0 && tid == 0) || (warp == wsel && lane == 0)) {
+                        if (c == 0) p.tokens[(int64_t)b * p.N + i] = y;
+                        s_tok[g] = y;
+                    }
                 }
                 __syncthreads();
             }
-            live = live && walk_barrier(ctr, timed_out, target += ncta);
         }
         // ---- statuses of the group (CTA 0); a stream that stopped early pads its tokens
         if (c == 0 && tid < gn) {
