@@ -88,7 +88,8 @@ def test_workspace_size_and_check(L):
     # one 16-byte partial per (row, stats segment <= 64); a stream has <= 2 kmax + 1 rows
     # one block per row: a 16-byte counter slot and 64 partials of 16 bytes
     # a 256-byte header, a 1536-byte block per stats row (at the same offset for every B and
-    # kmax), then the residual sweep's work list: 32 bytes per claim, 32 claims per slot
+    # kmax), then the residual sweep's work list: 32 bytes per claim, one claim per segment
+    # (64 per slot)
     assert sv.spec_verify_workspace_bytes(64, 5) == 256 + 64 * 11 * 1536 + 64 * 6 * 64 * 32
     for B, kmax in ((1, 0), (7, 3), (256, 15), (3, 32)):
         assert sv.spec_verify_workspace_bytes(B, kmax) == 256 + B * (2 * kmax + 1) * 1536 + B * (kmax + 1) * 2048
@@ -106,3 +107,19 @@ def test_workspace_size_and_check(L):
     assert L.spec_verify_tokenwise(ctypes.byref(a), None) == -6
     a.workspace, a.workspace_bytes = 4104, 1 << 20   # not 16-byte aligned
     assert L.spec_verify_block(ctypes.byref(a), None) == -6
+
+
+def test_walk_workspace_size_and_check(L):
+    # the barrier counter and timeout flag (256 bytes), then every CTA's 16-byte partial per
+    # stream (up to 2048 CTAs) in two buffers that alternate from slot to slot
+    for B in (1, 4, 33):
+        assert L.dspark_markov_walk_workspace_bytes(B) == 256 + 2 * B * 2048 * 16
+    assert L.dspark_markov_walk_workspace_bytes(-1) == 0
+    vp = ctypes.c_void_p
+    p = vp(4096)   # never dereferenced: the workspace check comes before any launch
+    need = L.dspark_markov_walk_workspace_bytes(2)
+    args = (p, 1, 2, 5, 1024, p, p, p, 1, 256, p, 0, 0, p, p, p)
+    assert L.dspark_markov_walk(*args, vp(4096), need - 1, vp(0)) == -6
+    assert b"workspace" in L.spec_last_error()
+    assert L.dspark_markov_walk(*args, vp(4104), need, vp(0)) == -6   # not 16-byte aligned
+    assert L.dspark_markov_walk(*args, None, need, vp(0)) == -6
