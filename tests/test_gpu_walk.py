@@ -128,3 +128,20 @@ def test_walk_then_verify_is_markov_consistent(rule):
         parity.compare_verify(g, o, inp["cu_drafts"], [0], np.array(r["tokens"]), inp["V"], check_diag=False)
         compared += 1
     assert compared >= 5
+
+
+@pytest.mark.parametrize("name,B", [("single_bias", 1), ("tiny", 9)])
+def test_walk_is_reproducible_call_to_call(name, B):
+    """Every CTA reduces the same partials and rescans the same drawn slice, with the partials
+    alternating between two buffers from slot to slot; the same inputs, seed and step must give
+    the same tokens, biased rows and statuses bit for bit, call after call (B = 9: three groups
+    of streams, so the buffers also turn over between groups)."""
+    host, dev = _inputs(name, 530, B=B, T=None if B == 1 else [1.0, 0.0, 0.7, 1.3, 1.0, 0.5, 1.1, 0.9, 0.0])
+    ref = {k: v.clone() for k, v in sv.dspark_markov_walk(dev["d"], dev["anchor"], dev["w1"], dev["w2"], dev["T"],
+                                                           3, 7).items() if k != "workspace"}
+    out = None
+    for _ in range(25):
+        out = sv.dspark_markov_walk(dev["d"], dev["anchor"], dev["w1"], dev["w2"], dev["T"], 3, 7, out=out)
+        for k, v in ref.items():
+            assert torch.equal(out[k].view(torch.int32) if out[k].dtype == torch.float32 else out[k],
+                               v.view(torch.int32) if v.dtype == torch.float32 else v), k
