@@ -9,7 +9,7 @@
 //   l~_i = l_i + W1[t_{i-1}] @ W2   (t_{-1} = the anchor),   t_i ~ softmax(l~_i / T)
 //
 // Design: one cooperative grid, one CTA per SM; CTA c owns a contiguous slice of the
-// vocabulary for the whole walk.  Per slot: the CTA gathers W1[t_{i-1}] of up to kWalkGroup
+// vocabulary for the whole walk.  Per slot: the CTA gathers W1[t_{i-1}] of up to WG (kWalkGroup, or 1 for a lone stream)
 // streams into shared memory and computes the biased logits of its slice - W2 (66 MB for rank
 // 256 at V = 129,280) is read once per slot for all streams of the group and stays in L2
 // between slots; the CTA's 8 warps split it as 4 column groups x 2 rank halves - writes them (they are the rows the verify's q is taken from) and publishes
@@ -109,22 +109,24 @@ __device__ bool walk_barrier(unsigned* ctr, unsigned* timed_out, unsigned target
     return ok != 0;
 }
 
-// Dynamic shared memory of a walk CTA: the group's W1 rows [kWalkGroup][R] floats, the rank
-// halves' meeting area [4][32][kWalkGroup][E] floats, then (16-byte aligned) one float4 per CTA
-// of the grid for the partials of the stream being drawn.
-__host__ __device__ inline size_t walk_parts_offset(int R, int E) {
-    const size_t b = sizeof(float) * ((size_t)kWalkGroup * R + (size_t)4 * 32 * kWalkGroup * E);
+// Dynamic shared memory of a walk CTA over groups of WG streams: the group's W1 rows [WG][R]
+// floats, the rank halves' meeting area [4][32][WG][E] floats, then (16-byte aligned) one float4
+// per CTA of the grid for the partials of the stream being drawn.
+__host__ __device__ inline size_t walk_parts_offset(int R, int E, int WG) {
+    const size_t b = sizeof(float) * ((size_t)WG * R + (size_t)4 * 32 * WG * E);
     return (b + 15) & ~(size_t)15;
 }
 
-template <typename DT, typename WT, int E>
+// WG streams walked together (each W2 element feeds all of them): WG, or 1 for a lone
+// stream, whose bias then issues a quarter of the FMAs.
+template <typename DT, typename WT, int E, int WG>
 __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams p) {
-    extern __shared__ __align__(16) float w1s[];   // [kWalkGroup][R], the reduction area, the CTAs' partials
-    __shared__ int s_prev[kWalkGroup], s_alive[kWalkGroup], s_greedy[kWalkGroup], s_status[kWalkGroup];
-    __shared__ float s_ah[kWalkGroup], s_al[kWalkGroup];
-    __shared__ float s_red[kWalkWarps][kWalkGroup][4];
+    extern __shared__ __align__(16) float w1s[];   // [WG][R], the reduction area, the CTAs' partials
+    __shared__ int s_prev[WG], s_alive[WG], s_greedy[WG], s_status[WG];
+    __shared__ float s_ah[WG], s_al[WG];
+    __shared__ float s_red[kWalkWarps][WG][4];
     __shared__ int s_draw_seg;
-    __shared__ int s_tok[kWalkGroup];   // the token each stream of the group drew at the current slot
+    __shared__ int s_tok[WG];   // the token each stream of the group drew at the current slot
     __shared__ unsigned long long s_sub[kWalkWarps], s_t, s_excl;
     __shared__ int s_sub_last[kWalkWarps];
     __shared__ float s_scale, s_K;
@@ -136,14 +138,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
     unsigned* timed_out = ctr + 1;
     WalkPart* parts = reinterpret_cast<WalkPart*>(p.ws + 256);
     // one stream's partials of every CTA, read from L2 once per draw by warp 0
-    float4* s_parts = reinterpret_cast<float4*>(reinterpret_cast<char*>(w1s) + walk_parts_offset(p.R, E));
+    float4* s_parts = reinterpret_cast<float4*>(reinterpret_cast<char*>(w1s) + walk_parts_offset(p.R, E, WG));
     unsigned target = 0;
     bool live = true;   // no barrier has given up
     const float qnan = __int_as_float(0x7fffffff);
 
-    for (int g0 = 0; g0 < p.B; g0 += kWalkGroup) {
-        const int gn = min(kWalkGroup, p.B - g0);
-        if (tid < kWalkGroup) {
+    for (int g0 = 0; g0 < p.B; g0 += WG) {
+        const int gn = min(WG, p.B - g0);
+        if (tid < WG) {
             const int b = g0 + tid;
             int st = SPEC_ST_OK;
             float ah = 0.f, al = 0.f;
@@ -170,22 +172,22 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
         for (int i = 0; i < p.N; ++i) {
             // ---- the previous tokens and the gathered W1 rows; a stream that has stopped
             // reports -1 for the rest of its slots
-            if (tid < kWalkGroup) {
+            if (tid < WG) {
                 const int b = g0 + tid;
                 if (c == 0 && tid < gn && !s_alive[tid]) p.tokens[(int64_t)b * p.N + i] = -1;
                 s_prev[tid] = (s_alive[tid] != 0) ? (i == 0 ? p.anchor[b] : s_tok[tid]) : 0;
             }
             __syncthreads();
-            for (int t = tid; t < kWalkGroup * p.R; t += kWalkThreads) {
+            for (int t = tid; t < WG * p.R; t += kWalkThreads) {
                 const int gi = t / p.R, j = t - gi * p.R;
                 w1s[t] = (gi < gn && s_alive[gi]) ? load_elem<WT>(p.W1, (int64_t)s_prev[gi] * p.R + j) : 0.f;
             }
             __syncthreads();
             // ---- biased logits of this CTA's slice, and their maximum
-            float mx[kWalkGroup];
-            int arg[kWalkGroup];
+            float mx[WG];
+            int arg[WG];
 #pragma unroll
-            for (int g = 0; g < kWalkGroup; ++g) {
+            for (int g = 0; g < WG; ++g) {
                 mx[g] = -kInf;
                 arg[g] = INT_MAX;
             }
@@ -196,13 +198,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
             const int half = warp >> 2, cgrp = warp & 3;
             const int jsplit = (p.R + 1) / 2;
             const int ja = half ? jsplit : 0, jb = half ? p.R : jsplit;
-            float* red = w1s + kWalkGroup * p.R;   // [4][32][kWalkGroup][E]
+            float* red = w1s + WG * p.R;   // [4][32][WG][E]
             for (int64_t cb = k0; cb < k1; cb += 4 * 32) {
                 const int64_t k = cb + cgrp * 32 + lane;
                 const bool act = k < k1;
-                float acc[kWalkGroup][E];
+                float acc[WG][E];
 #pragma unroll
-                for (int g = 0; g < kWalkGroup; ++g)
+                for (int g = 0; g < WG; ++g)
 #pragma unroll
                     for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
                 if (act) {
@@ -213,28 +215,28 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                         float x[E];
                         cwv.unpack(x);
 #pragma unroll
-                        for (int g = 0; g < kWalkGroup; ++g) {
+                        for (int g = 0; g < WG; ++g) {
                             const float wv = w1s[g * p.R + j];
 #pragma unroll
                             for (int e = 0; e < E; ++e) acc[g][e] = fmaf(wv, x[e], acc[g][e]);
                         }
                     }
                 }
-                float* rl = red + ((cgrp * 32 + lane) * kWalkGroup) * E;
+                float* rl = red + ((cgrp * 32 + lane) * WG) * E;
                 if (half) {
 #pragma unroll
-                    for (int g = 0; g < kWalkGroup; ++g)
+                    for (int g = 0; g < WG; ++g)
 #pragma unroll
                         for (int e = 0; e < E; ++e) rl[g * E + e] = acc[g][e];
                 }
                 __syncthreads();   // the upper half's sums are in shared memory
                 if (!half && act) {
 #pragma unroll
-                    for (int g = 0; g < kWalkGroup; ++g)
+                    for (int g = 0; g < WG; ++g)
 #pragma unroll
                         for (int e = 0; e < E; ++e) acc[g][e] += rl[g * E + e];
 #pragma unroll
-                    for (int g = 0; g < kWalkGroup; ++g) {
+                    for (int g = 0; g < WG; ++g) {
                         if (g >= gn) continue;
                         const int64_t row = ((int64_t)(g0 + g) * p.N + i);
                         Chunk<DT, E> cd;
@@ -258,7 +260,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
             }
             // CTA maximum (NaN-aware) and its lowest index, per stream
 #pragma unroll
-            for (int g = 0; g < kWalkGroup; ++g) {
+            for (int g = 0; g < WG; ++g) {
                 const float m = warp_max_nan(mx[g]);
                 const int a = warp_min_i(mx[g] == m ? arg[g] : INT_MAX);
                 if (lane == 0) {
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                 }
             }
             __syncthreads();
-            if (tid < kWalkGroup) {
+            if (tid < WG) {
                 float m = -kInf;
                 for (int w = 0; w < kWalkWarps; ++w) m = fmax_nan(m, s_red[w][tid][0]);
                 int a = INT_MAX;
@@ -279,17 +281,17 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
             __syncthreads();
             // ---- T > 0: sum 2^(l~ a - K) over the slice (K = ceil of the slice maximum); the
             // biased values are read back from the output this CTA just wrote
-            float kref[kWalkGroup];
-            df sum[kWalkGroup];
+            float kref[WG];
+            df sum[WG];
 #pragma unroll
-            for (int g = 0; g < kWalkGroup; ++g) {
+            for (int g = 0; g < WG; ++g) {
                 const float m = s_red[0][g][2];
                 kref[g] = (isfinite(m)) ? ceilf(m) : kWalkNoRef;
                 sum[g] = df{0.f, 0.f};
             }
             for (int64_t k = k0 + tid; k < k1; k += kWalkThreads) {
 #pragma unroll
-                for (int g = 0; g < kWalkGroup; ++g) {
+                for (int g = 0; g < WG; ++g) {
                     if (g >= gn || s_greedy[g] || !s_alive[g]) continue;
                     const float* o = p.out + ((int64_t)(g0 + g) * p.N + i) * V + k * E;
                     float t = 0.f;
@@ -302,7 +304,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
                 }
             }
 #pragma unroll
-            for (int g = 0; g < kWalkGroup; ++g) {
+            for (int g = 0; g < WG; ++g) {
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) {
                     const df other{__shfl_xor_sync(0xffffffffu, sum[g].hi, o), __shfl_xor_sync(0xffffffffu, sum[g].lo, o)};
@@ -500,15 +502,15 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_kernel(const WalkParams 
     }
 }
 
-template <typename DT, typename WT, int E>
-static cudaError_t launch_walk(WalkParams& p, cudaStream_t s) {
+template <typename DT, typename WT, int E, int WG>
+static cudaError_t launch_walk_wg(WalkParams& p, cudaStream_t s) {
     static std::atomic<int> grid_cache[64];   // per device: the cooperative grid (0: not yet set up)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
     int grid = grid_cache[dev].load(std::memory_order_acquire);
     if (grid == 0) {
-        cudaError_t e = cudaFuncSetAttribute(walk_kernel<DT, WT, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(walk_parts_offset(kWalkMaxRank, E) + sizeof(float4) * kWalkMaxCtas));
+        cudaError_t e = cudaFuncSetAttribute(walk_kernel<DT, WT, E, WG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(walk_parts_offset(kWalkMaxRank, E, WG) + sizeof(float4) * kWalkMaxCtas));
         if (e != cudaSuccess) return e;
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
@@ -516,13 +518,18 @@ static cudaError_t launch_walk(WalkParams& p, cudaStream_t s) {
         grid_cache[dev].store(grid, std::memory_order_release);
     }
     p.cw = (p.nchunk + grid - 1) / grid;
-    const size_t smem = walk_parts_offset(p.R, E) + sizeof(float4) * (size_t)grid;
+    const size_t smem = walk_parts_offset(p.R, E, WG) + sizeof(float4) * (size_t)grid;
     // the barrier counter and timeout flag start at zero in every launch
     cudaError_t e = cudaMemsetAsync(p.ws, 0, 8, s);
     if (e != cudaSuccess) return e;
     void* args[] = {&p};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(walk_kernel<DT, WT, E>), dim3(grid),
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(walk_kernel<DT, WT, E, WG>), dim3(grid),
                                        dim3(kWalkThreads), args, smem, s);
+}
+
+template <typename DT, typename WT, int E>
+static cudaError_t launch_walk(WalkParams& p, cudaStream_t s) {
+    return p.B == 1 ? launch_walk_wg<DT, WT, E, 1>(p, s) : launch_walk_wg<DT, WT, E, kWalkGroup>(p, s);
 }
 
 template <int E>
