@@ -129,7 +129,7 @@ int dspark_markov_bias(const void* draft_logits, int32_t draft_dtype, int32_t ro
  * NaN, +inf or no finite entry; the stream stops there), TIMEOUT (a bounded grid wait gave up).
  * workspace: dspark_markov_walk_workspace_bytes(B) bytes of device scratch, 16-byte aligned,
  * any contents (the call clears what it needs).  One cooperative launch: N slots for every
- * group of four streams, one grid-wide barrier per slot.
+ * group of four streams (one stream alone: a group of one), one grid-wide barrier per slot.
  * Errors: SPEC_ERR_ARG (NULL pointer), SPEC_ERR_DTYPE, SPEC_ERR_SHAPE (B < 0, N outside
  * [0, SPEC_MAX_KMAX], V outside [1, SPEC_MAX_V], rank outside [1, 1024]), SPEC_ERR_WORKSPACE,
  * SPEC_ERR_CUDA.  B == 0 launches nothing.
